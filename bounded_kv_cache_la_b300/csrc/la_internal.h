@@ -1,0 +1,185 @@
+// Internal declarations shared by the host state machine (la_cache.cu) and
+// the kernels.  Not part of the public ABI (include/la_cache.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/la_cache.h"
+
+namespace la {
+
+constexpr int kMaxExact = LA_MAX_SLOTS;   // exact slots (cached blocks + current)
+constexpr int kMaxAttnSlots = kMaxExact + 1;  // + ConvKV memory slot
+
+enum SlotKind : int { SLOT_FRAME = 0, SLOT_CURRENT = 1, SLOT_MEMORY = 2 };
+
+// Device error word.  code: 0 ok, LA_ERR_DEVICE or LA_ERR_TIMEOUT; the first
+// fault wins (atomicCAS on code).
+struct DevError {
+  int code;
+  int kernel;   // KernelId
+  int detail0;
+  int detail1;
+};
+enum KernelId : int {
+  KID_RETRIEVAL = 1, KID_APPEND = 2, KID_CONVKV = 3, KID_ATTN_SIMT = 4, KID_ATTN_TC = 5,
+  KID_QROT = 6, KID_INIT = 7
+};
+
+// Slot table of the block being generated.  Written by the host at select,
+// read by every attention kernel of the block.
+struct DevContext {
+  int n_slots;                     // attention slots (memory + exact)
+  int kv_len;
+  int t0_cur;                      // temporal base of the current block
+  int block;
+  int kind[kMaxAttnSlots];
+  int frame[kMaxAttnSlots];        // frame index for SLOT_FRAME, else -1
+  int tokens[kMaxAttnSlots];
+  int t0[kMaxAttnSlots];
+};
+
+// Retrieval results (top k+1 in descending order).
+struct DevTopk {
+  unsigned int done;               // CTA completion counter (reset by the last CTA)
+  int n;                           // entries written (<= k + 1)
+  int ids[LA_MAX_TOPK + 1];
+  float scores[LA_MAX_TOPK + 1];
+};
+
+// Byte offsets of every region inside the caller's pool.
+struct Layout {
+  size_t err, ctx, topk;           // control
+  size_t amax;                     // e4m3 amax scratch [2][H] uint32
+  size_t pose_tab;                 // [max_history][36] fp32
+  size_t inv_norm;                 // [max_history] fp32
+  size_t scores;                   // retrieval scratch [max_history] fp32
+  size_t rope_t, rope_h, rope_w;   // float2 (cos, sin) tables
+  size_t scales;                   // e4m3 [L][n_frames][2][H] fp32
+  size_t cur_scales;               // e4m3 [2][H] fp32
+  size_t frames;                   // [L][n_frames][G] pages
+  size_t cur_pages;                // 2 pages: current block K', V
+  size_t qrot;                     // [S][H][T][D] bf16 rotated queries (tensor path)
+  size_t mem;                      // ConvKV [L][3][H][cap][D] bf16 (raw K, V, rotated K)
+  size_t total;
+  size_t page_bytes;               // H * T * D * elt(kv_dtype)
+  size_t page_stride;              // page_bytes rounded up to 1024
+  int G;                           // pages per frame: 2 (K', V) or 3 (+ raw K)
+  int n_frames;                    // frames per layer
+  int max_t;                       // rows of the temporal RoPE table
+  int n_qrot;                      // rotated-query slots held
+  int T;
+};
+
+struct RopeDims {
+  int dt, dh, dw;                  // dims per axis
+  int F, GH, GW;                   // block grid
+  int max_t;                       // rows of tab_t
+  const float2* tab_t;             // [max_t][dt/2]
+  const float2* tab_h;             // [GH][dh/2]
+  const float2* tab_w;             // [GW][dw/2]
+};
+
+// ------------------------------------------------------------ kernel launches
+// Each returns the cudaError_t of its launch(es).
+cudaError_t launch_init_tables(float2* tab_t, int max_t, int dt, float2* tab_h, int GH, int dh,
+                               float2* tab_w, int GW, int dw, double theta, cudaStream_t s);
+
+struct RetrievalArgs {
+  float kp[34];
+  int pose_row;        // table row for the query descriptor, -1 = none
+  int c0, c1;          // candidate ids [c0, c1)
+  int k;               // picks (<= LA_MAX_TOPK); k + 1 are ranked
+  int max_history;
+  float* table;        // [max_history][36]
+  float* inv_norm;
+  float* scores;
+  DevTopk* topk;
+  DevError* err;
+};
+cudaError_t launch_retrieval(const RetrievalArgs& a, cudaStream_t s);
+
+struct AppendArgs {
+  const void* k;       // [T][H][D] src_dtype
+  const void* v;
+  void* k_dst;         // [H][T][D] dst_dtype, RoPE'd by the within-block position
+  void* v_dst;
+  void* kraw_dst;      // optional [H][T][D] un-rotated copy (ConvKV)
+  float* k_scale;      // e4m3: [H]
+  float* v_scale;
+  unsigned int* amax;  // e4m3 scratch [2][H]
+  int T, H, D;
+  int src_dtype, dst_dtype;
+  RopeDims rope;
+  DevError* err;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+
+struct ConvArgs {
+  const void* kraw;    // evicted block [H][T][D] bf16
+  const void* v;
+  const void* w;       // [2][H][D][R] bf16
+  void* k_ring;        // [H][cap][D] bf16
+  void* v_ring;
+  void* krot_ring;
+  int T, H, D, R, stride, n_out, cap;
+  int write0;          // ring index of the first new token
+  int n_after, head_after;   // memory tokens and oldest ring index after the append
+  RopeDims rope;
+  DevError* err;
+};
+cudaError_t launch_convkv(const ConvArgs& a, cudaStream_t s);
+
+struct AttnArgs {
+  const void* q;       // [T][H][D] q_dtype
+  void* out;           // [T][H][D] q_dtype
+  int T, H, D, q_dtype, kv_dtype;
+  const DevContext* ctx;
+  const char* frames;  // layer's first frame page
+  size_t page_stride;
+  int G;
+  int n_frames;        // frames per layer (bound of ctx->frame)
+  const char* cur_k;   // current block pages
+  const char* cur_v;
+  const float* frame_scales;  // e4m3: this layer's [n_frames][2][H]
+  const float* cur_scales;    // e4m3: [2][H]
+  const char* mem_krot;       // this layer's ConvKV rotated keys [H][cap][D]
+  const char* mem_v;
+  int mem_cap;
+  float scale;
+  RopeDims rope;
+  DevError* err;
+};
+cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t s);
+
+struct QrotArgs {
+  const void* q;       // [T][H][D] bf16
+  void* qrot;          // [S][H][T][D] bf16
+  const DevContext* ctx;
+  int T, H, D, n_qrot;
+  RopeDims rope;
+  DevError* err;
+};
+cudaError_t launch_qrot(const QrotArgs& a, cudaStream_t s);
+
+struct TcAttnArgs {
+  CUtensorMap tm_q;    // rotated queries  [S*H][T][D] bf16
+  CUtensorMap tm_kv;   // pool pages       [frames*G*H][T][D] bf16 (whole pool)
+  CUtensorMap tm_cur;  // current pages    [2*H][T][D]
+  CUtensorMap tm_mem;  // ConvKV rings     [L*3*H][cap][D] (or a dummy)
+  const DevContext* ctx;
+  void* out;           // [T][H][D] bf16
+  int T, H;
+  int layer_frame0;    // first frame page row of this layer in tm_kv, in pages
+  int G;
+  int mem_row0;        // first row (in H-units) of this layer's rings in tm_mem
+  float scale_log2;
+  DevError* err;
+};
+cudaError_t launch_attn_tc(const TcAttnArgs& a, int num_sms, cudaStream_t s);
+bool attn_tc_supported(int D, int kv_dtype);
+
+}  // namespace la

@@ -1,0 +1,217 @@
+/*
+ * la_cache.h -- C ABI of the bounded KV cache and its block-causal chunk
+ * attention (single GPU, sm_103a).
+ *
+ * What the calls compute follows two pages on streaming video DiTs:
+ *   [LA]  "LiveAnimate: 实时稳定长时流式人体动画" (ai-feeds.com), 方法 / 实验:
+ *         PR-Sink bounded cache = static sink (first generated block, kept
+ *         forever) + dynamic sink (history blocks retrieved by pose
+ *         similarity) + rolling window of the 3 most recent blocks; each block
+ *         attends only to the reference and earlier blocks; cache size and
+ *         per-block latency stay constant as the stream grows.
+ *   [LX]  "Soul App开源实时数字人生成框架SoulX-LiveAct详解" (youleyou.com),
+ *         技术内核 / 上手实践指南: ConvKV memory (recent K/V exact, older K/V
+ *         compressed about 5:1 by a 1D convolution into fixed-length memory
+ *         with RoPE positions reset) and an FP8 KV cache.
+ *
+ * Conventions for every call
+ *   - Pointers named "device" must be CUDA device memory of the current
+ *     device; "host" pointers are ordinary host memory.  The library never
+ *     allocates device memory: the caller hands it one pool
+ *     (la_cache_required_bytes) and owns every input and output buffer.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued on it; device buffers passed in must stay
+ *     valid until that work completes.
+ *   - Q/K/V/O tensors of one block are row-major [T][H][D]: T tokens in
+ *     raster order (frame, row, column), H heads, D head dim; element type
+ *     `q_dtype` (LA_F32 or LA_BF16).
+ *   - Errors: arguments and call order are checked synchronously and the
+ *     status is returned.  Faults seen inside kernels (an index out of range,
+ *     a wait that ran out of time) are latched in a device error word that
+ *     la_get_error reads; after any error every call but la_get_error and
+ *     la_cache_destroy returns LA_ERR_STATE.
+ */
+#ifndef LA_CACHE_H
+#define LA_CACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LA_OK = 0,
+  LA_ERR_INVALID_ARG = 1,   /* bad pointer, size or configuration            */
+  LA_ERR_OOM = 2,           /* pool smaller than la_cache_required_bytes     */
+  LA_ERR_CUDA = 3,          /* a CUDA runtime call failed                    */
+  LA_ERR_STATE = 4,         /* call out of order, or an earlier error latched*/
+  LA_ERR_TIMEOUT = 5,       /* a device-side wait ran out of time            */
+  LA_ERR_UNSUPPORTED = 6,   /* valid but not built (shape/dtype combination) */
+  LA_ERR_DEVICE = 7         /* a kernel reported an out-of-range index       */
+} la_status;
+
+typedef enum { LA_POLICY_PR_SINK = 0, LA_POLICY_CONVKV = 1 } la_policy;
+typedef enum { LA_F32 = 0, LA_BF16 = 1, LA_E4M3 = 2 } la_dtype;
+
+/* Where history blocks that left the window live.
+ * RESIDENT: every appended block keeps its K/V pages in the pool, so any of
+ *   them can be retrieved into the dynamic sink without help.
+ * EXTERNAL: the pool holds only the attended blocks; when the dynamic sink
+ *   picks a history block, the caller supplies its K/V with la_fill_block
+ *   (the pages bound only the attended cache, [LA] 实验; history storage is
+ *   left to the caller). */
+typedef enum { LA_HISTORY_RESIDENT = 0, LA_HISTORY_EXTERNAL = 1 } la_history_mode;
+
+/* Attention kernel choice: AUTO = tensor cores where the shape is built
+ * for them (bf16/e4m3, D = 128), otherwise the CUDA-core kernel. */
+typedef enum { LA_ATTN_AUTO = 0, LA_ATTN_TENSOR = 1, LA_ATTN_SIMT = 2 } la_attn_impl;
+
+typedef struct {
+  int32_t num_layers, num_heads, head_dim;       /* L, H, D (D = 64 or 128)           */
+  int32_t frames_per_block, grid_h, grid_w;      /* T = F * GH * GW tokens per block  */
+  int32_t rope_t, rope_h, rope_w;                /* RoPE dims per axis, sum = D       */
+  float   rope_theta;                            /* 10000                              */
+  int32_t policy;                                /* la_policy                          */
+  int32_t static_sink;                           /* 1 = block 0 kept forever [LA]      */
+  int32_t dyn_topk;                              /* k of the dynamic sink, <= 8        */
+  int32_t window;                                /* rolling window, 3 in [LA]          */
+  int32_t pose_dim;                              /* 34 = 17 keypoints x (x, y)         */
+  int32_t max_history;                           /* blocks the pose table can hold     */
+  int32_t conv_kernel, conv_stride, mem_slots;   /* ConvKV: 5, 5, 4096 [LX]            */
+  int32_t q_dtype, kv_dtype;                     /* la_dtype                           */
+  float   softmax_scale;                         /* 1/sqrt(D)                          */
+  int32_t history_mode;                          /* la_history_mode                    */
+  int32_t attn_impl;                             /* la_attn_impl                       */
+} la_cache_config;
+
+#define LA_MAX_SLOTS 16
+#define LA_MAX_TOPK 8
+
+/* The context of the block being generated, in slot order:
+ * [static sink, dynamic sink (ascending id), window (oldest first), current]
+ * for PR-Sink; [window (oldest first), current] after `mem_tokens`
+ * compressed memory tokens for ConvKV. */
+typedef struct {
+  int32_t block;                       /* id of the block being generated      */
+  int32_t n_slots;                     /* exact slots, current block included  */
+  int32_t kv_len;                      /* keys attended: mem_tokens + n_slots*T */
+  int32_t mem_tokens;                  /* ConvKV memory tokens (0 for PR-Sink)  */
+  int32_t block_id[LA_MAX_SLOTS];      /* block held by each exact slot         */
+  int32_t t0[LA_MAX_SLOTS];            /* temporal RoPE base of each slot       */
+  int32_t n_dyn;                       /* dynamic-sink blocks chosen            */
+  int32_t dyn_ids[LA_MAX_TOPK];        /* ascending                             */
+  float   dyn_scores[LA_MAX_TOPK];     /* cosine score of each chosen block     */
+  float   topk_gap;                    /* score_k - score_(k+1); +inf if none   */
+  int32_t need_fill[LA_MAX_TOPK];      /* EXTERNAL: 1 = la_fill_block required   */
+} la_context;
+
+typedef struct la_cache la_cache_t;
+
+/* Device bytes the pool must have for `cfg` (0 if `cfg` is invalid). */
+size_t la_cache_required_bytes(const la_cache_config* cfg);
+
+/* Creates a cache inside `dev_pool` (device, >= la_cache_required_bytes,
+ * 256-byte aligned, owned by the caller and borrowed until destroy).
+ * `conv_w` (device, ConvKV only, else NULL): bf16 depthwise weights laid out
+ * [L][2 (K, V)][H][D][conv_kernel], borrowed until destroy.  Initialises the
+ * pool on `stream`.  On success *out receives the handle. */
+la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t pool_bytes,
+                          const void* conv_w, void* stream, la_cache_t** out);
+
+/* Releases the host state.  Synchronises `stream`-less: call it only after
+ * the work of the cache has completed.  The pool stays the caller's. */
+la_status la_cache_destroy(la_cache_t* cache);
+
+/* Starts block b (b = number of blocks appended so far).  Runs the pose
+ * retrieval kernel on `stream` ([LA] 方法, Dynamic Sink): the centred 34-value
+ * descriptor of `query_pose` (host, 17 (x, y) keypoints) is scored by cosine
+ * similarity against every history block that is neither the static sink,
+ * nor in the window, nor block b, and the top-k under (score desc, id asc)
+ * are taken.  Builds the slot table the attention reads.  Synchronises
+ * `stream` once to read the k chosen ids.  `out` (host, optional) receives
+ * the context. */
+la_status la_select_context(la_cache_t* cache, const float* query_pose, la_context* out,
+                            void* stream);
+
+/* EXTERNAL history only: writes the K/V of history block `block_id` for
+ * `layer` into the dynamic-sink page the last la_select_context gave it
+ * (need_fill = 1).  k, v: device [T][H][D] q_dtype, the block's final K/V as
+ * la_cache_append_block received them. */
+la_status la_fill_block(la_cache_t* cache, int layer, int block_id, const void* k,
+                        const void* v, void* stream);
+
+/* Block-causal chunk attention of the current block for one layer
+ * ([LA] 方法): every query token of the block attends, without mask, to all
+ * tokens of the context (memory, cached slots and the current block itself).
+ * 3D RoPE over (t, h, w) positions is applied to queries and keys; the slot
+ * at temporal base t0 holds positions (t0 + frame, row, column).
+ * q, k_cur, v_cur: device [T][H][D] q_dtype (the current block's values at
+ * this denoising step); out: device [T][H][D] q_dtype.
+ * out = softmax(softmax_scale * RoPE(q) RoPE(K_ctx)^T) V_ctx, per head. */
+la_status la_chunk_attention(la_cache_t* cache, int layer, const void* q, const void* k_cur,
+                             const void* v_cur, void* out, void* stream);
+
+/* Appends the current block's final K/V for `layer` (device [T][H][D]
+ * q_dtype).  When every layer has been appended the block is committed: its
+ * pose joins the history, the window rolls ([LA] 方法, Rolling Window) and,
+ * for ConvKV, the block leaving the window is compressed into the memory
+ * ([LX] 技术内核) -- the compression of each layer runs in that layer's
+ * append.  For an e4m3 cache the K/V are quantised with one fp32 scale per
+ * (head, block). */
+la_status la_cache_append_block(la_cache_t* cache, int layer, const void* k, const void* v,
+                                void* stream);
+
+/* Called by la_stream_step for each (layer, block) needing a fill. */
+typedef la_status (*la_fill_fn)(la_cache_t* cache, int layer, int block_id, void* user,
+                                void* stream);
+
+/* One streamed block: select, n_steps x L chunk attentions, then L appends
+ * of the last step's K/V.  q, k, v, out: host arrays of n_steps*L device
+ * pointers, entry [step * L + layer].  `fill` (required in EXTERNAL mode
+ * when a fill is needed) is called between select and the attentions. */
+la_status la_stream_step(la_cache_t* cache, const float* pose, int n_steps,
+                         const void* const* q, const void* const* k, const void* const* v,
+                         void* const* out, la_fill_fn fill, void* user, void* stream);
+
+/* EXTERNAL history only: loads the pose history of blocks 0..n-1 (host,
+ * n x 17 x 2 keypoints) into an empty cache, as when a stream resumes with
+ * its K/V held by the caller; the next block is n.  Blocks n-window..n-1
+ * must then be supplied with la_fill_window before attention. */
+la_status la_cache_load_history(la_cache_t* cache, const float* kps, int n, void* stream);
+
+/* EXTERNAL history after la_cache_load_history: writes the K/V of a block
+ * that is the static sink or in the window (device [T][H][D]). */
+la_status la_fill_window(la_cache_t* cache, int layer, int block_id, const void* k,
+                         const void* v, void* stream);
+
+/* Synchronises the device, reads the device error word and writes a
+ * message (host, `cap` bytes) -- LA_OK if no kernel reported a fault. */
+la_status la_get_error(la_cache_t* cache, char* msg, size_t cap);
+
+/* Host only, no device work: the context of block `block` given the chosen
+ * dynamic ids (ascending, n_dyn of them).  Lets callers and tests check the
+ * slot order and RoPE bases without a GPU. */
+la_status la_context_plan(const la_cache_config* cfg, int block, const int32_t* dyn_ids,
+                          int n_dyn, la_context* out);
+
+/* Test access to stored pages.  Returns the device address of the page
+ * holding `which` (0 = RoPE'd key, 1 = value, 2 = raw key [ConvKV]) of
+ * `block_id` for `layer`, laid out [H][T][D] in kv_dtype, and for e4m3 the
+ * device address of its H fp32 scales (else NULL). */
+la_status la_debug_page(la_cache_t* cache, int layer, int block_id, int which,
+                        void** page, void** scales);
+
+/* Test access to the ConvKV memory of `layer`: device addresses of the raw
+ * key ring, the value ring and the rotated key ring ([H][mem_slots][D] bf16),
+ * the number of valid tokens and the ring index of the oldest token. */
+la_status la_debug_memory(la_cache_t* cache, int layer, void** k_raw, void** v, void** k_rot,
+                          int* n_tokens, int* oldest);
+
+const char* la_status_string(la_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LA_CACHE_H */

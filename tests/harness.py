@@ -1,0 +1,127 @@
+"""Shared helpers of the GPU parity tests: seeded inputs on both sides,
+driving a stream through the C ABI, and the oracle's side of each check."""
+from __future__ import annotations
+
+import numpy as np
+
+from bounded_kv_cache_la_b300 import capi
+from oracle import stream as ostream
+from synth import gen
+
+# Tolerances.  bf16 / fp8: the bounds the workloads state (max-abs, mean-abs)
+# plus a relative L2 bound derived from the arithmetic (bf16 operands and
+# probabilities carry 2^-9 relative rounding; over many keys the output's
+# relative error stays well under 1e-2).
+TOL = {
+    "f32": dict(max_abs=2e-5, mean_abs=2e-6, rel=1e-4),
+    "bf16": dict(max_abs=2e-2, mean_abs=2e-3, rel=1.5e-2),
+    "e4m3": dict(max_abs=8e-2, mean_abs=8e-3, rel=3e-2),
+}
+
+
+def compare(got: np.ndarray, ref: np.ndarray, kind: str, what: str = ""):
+    t = TOL[kind]
+    d = np.abs(np.asarray(got, np.float64) - ref)
+    rel = np.linalg.norm(d) / max(np.linalg.norm(ref), 1e-30)
+    msg = f"{what}: max {d.max():.3e} mean {d.mean():.3e} rel {rel:.3e}"
+    assert d.max() <= t["max_abs"], msg
+    assert d.mean() <= t["mean_abs"], msg
+    assert rel <= t["rel"], msg
+    return d.max(), d.mean(), rel
+
+
+def head_index(T: int, H: int, D: int, heads) -> np.ndarray:
+    t = np.arange(T)[:, None, None]
+    h = np.asarray(heads)[None, :, None]
+    d = np.arange(D)[None, None, :]
+    return ((t * H + h) * D + d).reshape(-1).astype(np.uint64)
+
+
+class Values:
+    """Seeded per-(layer, block, step) Q/K/V on the CPU (NumPy) for the oracle,
+    optionally restricted to a subset of heads."""
+
+    def __init__(self, sc, heads=None):
+        self.sc = sc
+        self.heads = heads
+        self._cache = {}
+
+    def get(self, layer, block, step, which):
+        key = (layer, block, step, which)
+        if key not in self._cache:
+            sc = self.sc
+            T, H, D = sc.tokens_per_block, sc.num_heads, sc.head_dim
+            k = gen.qkv_key(sc, layer, block, step, which)
+            if self.heads is None:
+                x = gen.tensor_np(k, (T, H, D), sc.qkv_dtype)
+            else:
+                idx = head_index(T, H, D, self.heads)
+                x = gen.tensor_np(k, None, sc.qkv_dtype, index_map=idx).reshape(T, len(self.heads), D)
+            self._cache[key] = x
+        return self._cache[key]
+
+    def kv_of(self, layer, step_of_block):
+        return lambda b: (self.get(layer, b, step_of_block(b), "k"),
+                          self.get(layer, b, step_of_block(b), "v"))
+
+
+def torch_values(sc, layer, block, step, device="cuda"):
+    T, H, D = sc.tokens_per_block, sc.num_heads, sc.head_dim
+    return [gen.tensor_torch(gen.qkv_key(sc, layer, block, step, w), (T, H, D), sc.qkv_dtype,
+                             device) for w in ("q", "k", "v")]
+
+
+def make_cache(sc, **kw):
+    import torch
+    cfg = capi.config_for(sc, **kw)
+    conv_w = None
+    if sc.policy == "convkv":
+        conv_w = torch.stack([gen.conv_weights_torch(sc, l, "cuda") for l in range(cfg.num_layers)])
+        conv_w = conv_w.contiguous()
+    return capi.Cache(cfg, conv_w=conv_w)
+
+
+def run_stream(sc, n_blocks, keep_blocks, *, n_steps=1, layers=1, cache=None, fill_values=True,
+               **cache_kw):
+    """Drives blocks 0..n_blocks-1 through the C ABI; returns (cache, contexts,
+    outputs) where outputs[b][(layer, step)] is the attention output (CPU
+    float32) for blocks in keep_blocks."""
+    import torch
+    sc_l = sc.with_(num_layers=layers)
+    if cache is None:
+        cache = make_cache(sc_l, **cache_kw)
+    kps = gen.poses(sc, n_blocks=n_blocks)
+    ctxs, outs = [], {}
+    for b in range(n_blocks):
+        ctx = cache.la_select_context(kps[b] if sc.policy == "prsink" else None)
+        ctxs.append(ctx)
+        if fill_values:
+            for i, bid in enumerate(ctx["dyn_ids"]):
+                if ctx["need_fill"][i]:
+                    for l in range(layers):
+                        _, k, v = torch_values(sc, l, bid, n_steps - 1)
+                        cache.la_fill_block(l, bid, k, v)
+        for s in range(n_steps):
+            for l in range(layers):
+                q, k, v = torch_values(sc, l, b, s)
+                out = torch.empty_like(q)
+                cache.la_chunk_attention(l, q, k, v, out)
+                if b in keep_blocks:
+                    outs.setdefault(b, {})[(l, s)] = out.float().cpu().numpy()
+        for l in range(layers):
+            _, k, v = torch_values(sc, l, b, n_steps - 1)
+            cache.la_cache_append_block(l, k, v)
+    torch.cuda.synchronize()
+    st, msg = cache.la_get_error()
+    assert st == capi.LA_OK, msg
+    return cache, ctxs, outs
+
+
+def oracle_output(sc, ctx, vals: Values, layer, step, n_steps, rows=None, w_kv=None):
+    """Oracle attention output of one call, context from the oracle's plan."""
+    kv_of = vals.kv_of(layer, lambda b: step if b == ctx.block else n_steps - 1)
+    mem = None
+    if ctx.mem_tokens:
+        mem = ostream.convkv_memory(sc, ctx.block, kv_of, w_kv)
+    q = vals.get(layer, ctx.block, step, "q")
+    return ostream.chunk_attention(sc, ctx, q, kv_of, mem=mem, rows=rows)

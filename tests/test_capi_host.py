@@ -1,0 +1,98 @@
+"""C-ABI library: loads, exports every declared symbol, and its host-only
+planning logic agrees with the oracle (no GPU needed)."""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from bounded_kv_cache_la_b300 import capi
+from oracle import stream
+from synth import C1_TINY, C2_MID, C3_14B, C4_CONVKV, C5_FP8, gen
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "la_cache.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = "\n".join(l for l in text.splitlines() if "typedef" not in l)
+    return set(re.findall(r"\b(la_[a-z_]+)\s*\(", text))
+
+
+def test_header_and_binding_agree():
+    assert _declared_functions() == set(capi.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", capi.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = _declared_functions() - exported
+    assert not missing, missing
+    for name in _declared_functions():
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.la_status_string(s)
+
+
+@pytest.mark.parametrize("sc", [C1_TINY, C2_MID, C3_14B, C4_CONVKV, C5_FP8])
+def test_required_bytes(sc):
+    cfg = capi.config_for(sc)
+    n = capi.la_cache_required_bytes(cfg)
+    assert n > 0
+    T, H, D = sc.tokens_per_block, sc.num_heads, sc.head_dim
+    elt = {"f32": 4, "bf16": 2, "e4m3": 1}[sc.kv_dtype]
+    page = T * H * D * elt
+    # at least every attended block's K and V for every layer
+    n_blocks = 1 + sc.dyn_topk + sc.window + 1 if sc.policy == "prsink" else sc.window + 1
+    assert n >= 2 * page * n_blocks * sc.num_layers
+    if sc is C3_14B:
+        assert n < 60e9          # bounded: independent of the 3600-block stream
+
+
+def test_invalid_configs_rejected():
+    cfg = capi.config_for(C2_MID)
+    cfg.rope_t += 2
+    assert capi.la_cache_required_bytes(cfg) == 0
+    cfg = capi.config_for(C2_MID)
+    cfg.dyn_topk = 20
+    assert capi.la_cache_required_bytes(cfg) == 0
+    cfg = capi.config_for(C2_MID)
+    cfg.head_dim = 96
+    assert capi.la_cache_required_bytes(cfg) == 0
+
+
+@pytest.mark.parametrize("sc,n", [(C1_TINY, 24), (C2_MID, 64), (C3_14B, 400), (C5_FP8, 300)])
+def test_plan_matches_oracle_prsink(sc, n):
+    cfg = capi.config_for(sc)
+    ctxs = stream.plan_stream(sc, gen.poses(sc, n_blocks=n), n)
+    for ctx in ctxs:
+        got = capi.la_context_plan(cfg, ctx.block, ctx.dyn_ids)
+        assert got["blocks"] == ctx.blocks
+        assert got["t0"] == ctx.t0
+        assert got["kv_len"] == ctx.kv_len
+        assert got["mem_tokens"] == 0
+
+
+def test_plan_matches_oracle_convkv():
+    sc = C4_CONVKV
+    cfg = capi.config_for(sc)
+    for b in range(0, 1000, 7):
+        ctx = stream.plan_convkv(sc, b)
+        got = capi.la_context_plan(cfg, b, [])
+        assert got["blocks"] == ctx.blocks
+        assert got["t0"] == ctx.t0
+        assert got["mem_tokens"] == ctx.mem_tokens
+        assert got["kv_len"] == ctx.kv_len
+
+
+def test_plan_rejects_bad_dynamic_ids():
+    cfg = capi.config_for(C2_MID)
+    for ids in ([0], [9], [3, 3], [50]):
+        with pytest.raises(capi.LaError):
+            capi.la_context_plan(cfg, 10, ids)

@@ -1,26 +1,497 @@
-// Tensor-core chunk attention (tcgen05 + TMEM + TMA).  Placeholder until the
-// kernel lands: reports the shape as unsupported so the CUDA-core kernel runs.
+// Fused gather + 3D-RoPE + flash attention on the tcgen05 tensor cores.
+//
+// "LiveAnimate" (ai-feeds.com) 方法: the current block attends, with no mask,
+// to its bounded context (static sink, pose-retrieved dynamic sink, window of
+// 3 blocks, itself); ConvKV ("SoulX-LiveAct" 技术内核) adds a compressed
+// memory whose positions restart at 0.  Per head:
+//     O = softmax(scale * R(Q) R(K_ctx)^T) V_ctx.
+//
+// RoPE.  Keys sit in the pool turned by their within-block position; the
+// per-slot temporal offset is moved to the query side (scores depend only on
+// position differences), so a query-rotation pass writes one rotated copy of
+// Q per slot and the attention kernel itself does no trigonometry.
+//
+// Gather.  K/V tiles are TMA-loaded straight from the slot's pool page (the
+// slot table says which page), 128 keys x 64 dims per box, 128-byte swizzle;
+// rows past a slot's end are zero-filled by TMA and masked to -inf.
+//
+// CTA = 2 query tiles of 128 rows of one head, persistent over (head, tile
+// pair) units.  12 warps:
+//   warp 0       TMA producer (K ring, V ring, per-slot Q tiles)
+//   warp 1       MMA issuer: S_i = Q_i K^T (smem x smem) into TMEM,
+//                O_i += P_i V (P from TMEM, V from smem, MN-major)
+//   warp 2       TMEM allocator
+//   warps 4..7   softmax of query tile 0 (one thread per row)
+//   warps 8..11  softmax of query tile 1
+// TMEM columns: S0 | S1 | O0 | O1 (128 each); P_i overwrites S_i as bf16.
+// Issue order PV0(j-1), QK0(j), PV1(j-1), QK1(j) lets each softmax run while
+// the tensor core works on the other tile.  Online softmax in base 2 with a
+// lazy rescale: the running max moves only when a row's max grows by more
+// than 8 (a factor 256), then O and l are rescaled in TMEM / registers.
+//
+// Every wait is bounded (2 s); on timeout the kernel latches LA_ERR_TIMEOUT,
+// drains its in-flight copies and MMAs, frees TMEM and returns.
 #include "dev_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace la {
 
-bool attn_tc_supported(int D, int kv_dtype) {
-  (void)D;
-  (void)kv_dtype;
-  return false;
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;                 // query rows per tile
+constexpr int kBN = 128;                 // keys per tile
+constexpr int kD = 128;                  // head dim
+constexpr int kTileBytes = kBM * kD * 2; // 32 KB: two 16 KB halves of 64 dims
+constexpr int kHalfBytes = kTileBytes / 2;
+constexpr int kKSt = 2, kVSt = 2;
+constexpr int kThreads = 384;
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
+constexpr int kOffV = kOffK + kKSt * kTileBytes;
+constexpr int kOffCtl = kOffV + kVSt * kTileBytes;
+constexpr int kCtlBytes = 1024;
+constexpr int kSmemBytes = kOffCtl + kCtlBytes + 1024;   // + alignment slack
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+// Register split: launched at 168 per thread (384 threads, 1 CTA per SM =
+// 64512).  Control warpgroup 128 x 72 + two softmax warpgroups 2 x 128 x 208
+// = 62464 <= 64512.
+constexpr int kRegsCtl = 72;
+constexpr int kRegsSoftmax = 208;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * 168, "register split too large");
+constexpr float kRescaleThreshold = 8.0f;                 // log2(256)
+
+struct Ctl {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kKSt], k_empty[kKSt];
+  uint64_t v_full[kVSt], v_empty[kVSt];
+  uint64_t s_full[2], p_ready[2], o_full[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  DevContext ctx;
+};
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block too large");
+
+struct Wait {
+  volatile int* abort_flag;
+  DevError* err;
+  __device__ __forceinline__ bool operator()(const uint64_t& bar, uint32_t parity, int where) const {
+    const uint32_t b = smem_u32(&bar);
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait(b, parity)) return true;
+      if ((it & 31) == 0) {
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+          *abort_flag = 1;
+          record_error(err, LA_ERR_TIMEOUT, KID_ATTN_TC, where, blockIdx.x);
+          return false;
+        }
+      }
+    }
+  }
+};
+
+// Tensor map and row of slot s's key (which = 0) or value (which = 1) pages.
+__device__ __forceinline__ const CUtensorMap* kv_map(const TcAttnArgs& a, const DevContext& c, int s,
+                                                     int which, int h, int& row) {
+  const int kind = c.kind[s];
+  if (kind == SLOT_FRAME) {
+    row = (a.layer_frame0 + c.frame[s] * a.G + which) * a.H + h;
+    return &a.tm_kv;
+  }
+  if (kind == SLOT_CURRENT) {
+    row = which * a.H + h;
+    return &a.tm_cur;
+  }
+  row = a.mem_row0 + (which == 0 ? 2 : 1) * a.H + h;     // rotated-key ring / value ring
+  return &a.tm_mem;
 }
 
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcAttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kOffCtl);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sQ = smem_u32(smem + kOffQ), sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&ctl.q_full), 1);
+    mbar_init(smem_u32(&ctl.q_empty), 1);
+    for (int i = 0; i < kKSt; ++i) {
+      mbar_init(smem_u32(&ctl.k_full[i]), 1);
+      mbar_init(smem_u32(&ctl.k_empty[i]), 1);
+    }
+    for (int i = 0; i < kVSt; ++i) {
+      mbar_init(smem_u32(&ctl.v_full[i]), 1);
+      mbar_init(smem_u32(&ctl.v_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctl.s_full[i]), 1);
+      mbar_init(smem_u32(&ctl.p_ready[i]), 128);
+      mbar_init(smem_u32(&ctl.o_full[i]), 1);
+    }
+    mbar_init(smem_u32(&ctl.mma_done), 1);
+    ctl.abort_flag = 0;
+    ctl.ctx = *a.ctx;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&ctl.tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&a.tm_q);
+    prefetch_tmap(&a.tm_kv);
+    prefetch_tmap(&a.tm_cur);
+    prefetch_tmap(&a.tm_mem);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const DevContext& cx = ctl.ctx;
+  const int n_slots = cx.n_slots;
+  bool bad = n_slots < 1 || n_slots > kMaxAttnSlots;
+  for (int s = 0; !bad && s < n_slots; ++s) {
+    const int k = cx.kind[s], tok = cx.tokens[s];
+    bad = tok < 1 || k < SLOT_FRAME || k > SLOT_MEMORY ||
+          (k == SLOT_FRAME && cx.frame[s] < 0) || (k != SLOT_MEMORY && tok > a.T);
+  }
+  const Wait wait{&ctl.abort_flag, a.err};
+  const uint32_t tmem = ctl.tmem_base;
+  const int n_pairs = (a.T + 2 * kBM - 1) / (2 * kBM);
+  const int n_units = a.H * n_pairs;
+  if (bad && tid == 0) record_error(a.err, LA_ERR_DEVICE, KID_ATTN_TC, n_slots, -1);
+
+  if (warp < 4) {
+   setmaxnreg_dec<kRegsCtl>();
+   if (bad) {
+   } else if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t kc = 0, vc = 0, qc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const int h = u / n_pairs, row0 = (u % n_pairs) * 2 * kBM;
+        for (int s = 0; ok && s < n_slots; ++s) {
+          const int nt = (cx.tokens[s] + kBN - 1) / kBN;
+          int krow, vrow;
+          const CUtensorMap* km = kv_map(a, cx, s, 0, h, krow);
+          const CUtensorMap* vm = kv_map(a, cx, s, 1, h, vrow);
+          for (int kt = 0; ok && kt < nt; ++kt) {
+            const int ks = kc % kKSt;
+            if (!(ok = wait(ctl.k_empty[ks], ((kc / kKSt) & 1) ^ 1, 1))) break;
+            mbar_arrive_expect_tx(smem_u32(&ctl.k_full[ks]), kTileBytes);
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(sK + ks * kTileBytes + hf * kHalfBytes, km, hf * 64, kt * kBN, krow,
+                          smem_u32(&ctl.k_full[ks]));
+            ++kc;
+            if (kt == 0) {
+              if (!(ok = wait(ctl.q_empty, (qc & 1) ^ 1, 2))) break;
+              mbar_arrive_expect_tx(smem_u32(&ctl.q_full), 2 * kTileBytes);
+              for (int i = 0; i < 2; ++i)
+                for (int hf = 0; hf < 2; ++hf)
+                  tma_load_3d(sQ + i * kTileBytes + hf * kHalfBytes, &a.tm_q, hf * 64,
+                              row0 + i * kBM, s * a.H + h, smem_u32(&ctl.q_full));
+              ++qc;
+            }
+            const int vs = vc % kVSt;
+            if (!(ok = wait(ctl.v_empty[vs], ((vc / kVSt) & 1) ^ 1, 3))) break;
+            mbar_arrive_expect_tx(smem_u32(&ctl.v_full[vs]), kTileBytes);
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(sV + vs * kTileBytes + hf * kHalfBytes, vm, hf * 64, kt * kBN, vrow,
+                          smem_u32(&ctl.v_full[vs]));
+            ++vc;
+          }
+        }
+      }
+      // Drain: the last loads issued on each ring must have landed before exit.
+      for (uint32_t i = (kc > kKSt ? kc - kKSt : 0); i < kc; ++i) {
+        const uint32_t b = smem_u32(&ctl.k_full[i % kKSt]);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(b, (i / kKSt) & 1) && globaltimer() - t0 < kTimeoutNs) {}
+      }
+      for (uint32_t i = (vc > kVSt ? vc - kVSt : 0); i < vc; ++i) {
+        const uint32_t b = smem_u32(&ctl.v_full[i % kVSt]);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(b, (i / kVSt) & 1) && globaltimer() - t0 < kTimeoutNs) {}
+      }
+      if (qc > 0) {
+        const uint32_t b = smem_u32(&ctl.q_full);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(b, (qc - 1) & 1) && globaltimer() - t0 < kTimeoutNs) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16(kBM, kBN, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16(kBM, kD, 0, 1);
+      uint32_t kc = 0, vc = 0, qc = 0, pc = 0;
+      bool ok = true;
+      auto issue_qk = [&](int i, int ks) {
+        const uint32_t q = sQ + i * kTileBytes, k = sK + ks * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss(tmem + i * 128, sdesc(q + off, 16, 1024), sdesc(k + off, 16, 1024), idesc_qk, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int i, int vs, bool first) {
+        const uint32_t v = sV + vs * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, sdesc(v + kk * 2048, kHalfBytes, 1024), idesc_pv,
+                 !(first && kk == 0));
+      };
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        int j = 0;
+        for (int s = 0; ok && s < n_slots; ++s) {
+          const int nt = (cx.tokens[s] + kBN - 1) / kBN;
+          for (int kt = 0; ok && kt < nt; ++kt, ++j) {
+            const int ks = kc % kKSt;
+            if (!(ok = wait(ctl.k_full[ks], (kc / kKSt) & 1, 11))) break;
+            tc_fence_after();
+            const int vs = vc % kVSt;
+            if (j > 0) {
+              if (!(ok = wait(ctl.p_ready[0], pc & 1, 12))) break;
+              if (!(ok = wait(ctl.v_full[vs], (vc / kVSt) & 1, 13))) break;
+              tc_fence_after();
+              issue_pv(0, vs, j == 1);
+            }
+            if (kt == 0) {
+              if (!(ok = wait(ctl.q_full, qc & 1, 14))) break;
+              tc_fence_after();
+              ++qc;
+            }
+            issue_qk(0, ks);
+            tc_commit(smem_u32(&ctl.s_full[0]));
+            if (j > 0) {
+              if (!(ok = wait(ctl.p_ready[1], pc & 1, 15))) break;
+              tc_fence_after();
+              issue_pv(1, vs, j == 1);
+              tc_commit(smem_u32(&ctl.v_empty[vs]));
+              ++vc;
+              ++pc;
+            }
+            issue_qk(1, ks);
+            tc_commit(smem_u32(&ctl.s_full[1]));
+            tc_commit(smem_u32(&ctl.k_empty[ks]));
+            ++kc;
+            if (kt == nt - 1) tc_commit(smem_u32(&ctl.q_empty));
+          }
+        }
+        if (!ok) break;
+        // last tile of the unit
+        const int vs = vc % kVSt;
+        if (!(ok = wait(ctl.p_ready[0], pc & 1, 16))) break;
+        if (!(ok = wait(ctl.v_full[vs], (vc / kVSt) & 1, 17))) break;
+        tc_fence_after();
+        issue_pv(0, vs, j == 1);
+        tc_commit(smem_u32(&ctl.o_full[0]));
+        if (!(ok = wait(ctl.p_ready[1], pc & 1, 18))) break;
+        tc_fence_after();
+        issue_pv(1, vs, j == 1);
+        tc_commit(smem_u32(&ctl.o_full[1]));
+        tc_commit(smem_u32(&ctl.v_empty[vs]));
+        ++vc;
+        ++pc;
+      }
+      // every MMA issued has completed before TMEM is released
+      tc_commit(smem_u32(&ctl.mma_done));
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(smem_u32(&ctl.mma_done), 0) && globaltimer() - t0 < kTimeoutNs) {}
+    }
+   }
+  } else {
+   setmaxnreg_inc<kRegsSoftmax>();
+   if (!bad) {
+    // ------------------------------------------------------------ softmax
+    const int i = (warp - 4) >> 2;                 // query tile of this warpgroup
+    const int quad = warp & 3;                     // TMEM lane quadrant of this warp
+    const int r = quad * 32 + lane;                // row within the tile
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + i * 128;
+    const uint32_t tO = tmem + lane_off + 256 + i * 128;
+    const float c = a.scale_log2;
+    uint32_t sph = 0, oph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+      const int h = u / n_pairs, row0 = (u % n_pairs) * 2 * kBM;
+      float m = -INFINITY, l = 0.f;
+      int j = 0;
+      for (int s = 0; ok && s < n_slots; ++s) {
+        const int tokens = cx.tokens[s];
+        const int nt = (tokens + kBN - 1) / kBN;
+        for (int kt = 0; kt < nt; ++kt, ++j) {
+          ok = __all_sync(0xffffffffu, wait(ctl.s_full[i], sph & 1, 21 + i));
+          if (!ok) break;
+          ++sph;
+          tc_fence_after();
+          float sv[kBN];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, reinterpret_cast<uint32_t*>(sv) + cc * 32);
+          tmem_wait_ld();
+          const int valid = tokens - kt * kBN;
+          if (valid < kBN) {
+#pragma unroll
+            for (int cc = 0; cc < kBN; ++cc)
+              if (cc >= valid) sv[cc] = -INFINITY;
+          }
+          float mx = sv[0];
+#pragma unroll
+          for (int cc = 1; cc < kBN; ++cc) mx = fmaxf(mx, sv[cc]);
+          mx *= c;
+          if (__any_sync(0xffffffffu, mx > m + kRescaleThreshold)) {
+            const float m_new = fmaxf(m, mx);
+            const float alpha = ex2(m - m_new);
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(tO + cc * 32, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                tmem_st32(tO + cc * 32, o);
+              }
+              tmem_wait_st();
+            }
+            l *= alpha;
+            m = m_new;
+          }
+          float sum = 0.f;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float p0 = ex2(fmaf(sv[half * 64 + 2 * e], c, -m));
+              const float p1 = ex2(fmaf(sv[half * 64 + 2 * e + 1], c, -m));
+              sum += p0 + p1;
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(tS + half * 32, pk);
+          }
+          l += sum;
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&ctl.p_ready[i]));
+        }
+      }
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, wait(ctl.o_full[i], oph & 1, 23 + i));
+      if (!ok) break;
+      ++oph;
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const int row = row0 + i * kBM + r;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + ((size_t)row * a.H + h) * kD;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc * 32, o);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+        if (row < a.T) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+      tc_fence_before();
+    }
+   }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Per-slot rotated copies of the queries: qrot[s][h][t] = R(t0_cur + f - t0_s, row, col) q[t][h].
+__global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
+  const DevContext& ctx = *a.ctx;
+  const int n_slots = ctx.n_slots;
+  if (n_slots < 1 || n_slots > a.n_qrot) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) record_error(a.err, LA_ERR_DEVICE, KID_QROT, n_slots, a.n_qrot);
+    return;
+  }
+  const int chunks = a.D / 8;
+  const long long total = (long long)a.T * a.H * chunks;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int cch = (int)(idx % chunks);
+    const long long th = idx / chunks;
+    const int h = (int)(th % a.H);
+    const int t = (int)(th / a.H);
+    uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + (size_t)th * a.D + cch * 8);
+    float x[8];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = __uint_as_float(w[e] << 16);
+      x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+    int f, hh, ww;
+    token_pos(a.rope, t, f, hh, ww);
+    for (int s = 0; s < n_slots; ++s) {
+      const int dtq = ctx.t0_cur + f - ctx.t0[s];
+      if (dtq < 0 || dtq >= a.rope.max_t) {
+        record_error(a.err, LA_ERR_DEVICE, KID_QROT, dtq, s);
+        return;
+      }
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 cs = rope_cs(a.rope, cch * 8 + 2 * e, dtq, hh, ww);
+        const float2 y = rot_exact(x[2 * e], x[2 * e + 1], cs);
+        ow[e] = pack_bf16x2(y.x, y.y);
+      }
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.qrot) +
+                                (((size_t)s * a.H + h) * a.T + t) * a.D + cch * 8) = o;
+    }
+  }
+}
+
+}  // namespace
+
+bool attn_tc_supported(int D, int kv_dtype) { return D == kD && kv_dtype == LA_BF16; }
+
 cudaError_t launch_qrot(const QrotArgs& a, cudaStream_t s) {
-  (void)a;
-  (void)s;
-  return cudaErrorNotSupported;
+  if (a.D % 8) return cudaErrorInvalidValue;
+  long long work = (long long)a.T * a.H * (a.D / 8);
+  long long grid = (work + 255) / 256;
+  if (grid > 148LL * 16) grid = 148LL * 16;
+  qrot_kernel<<<(int)grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attn_tc(const TcAttnArgs& a, int num_sms, cudaStream_t s) {
-  (void)a;
-  (void)num_sms;
-  (void)s;
-  return cudaErrorNotSupported;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int n_pairs = (a.T + 2 * kBM - 1) / (2 * kBM);
+  const int units = a.H * n_pairs;
+  const int grid = units < num_sms ? units : num_sms;
+  attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace la

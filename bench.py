@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Streamed-block benchmark of the bounded-KV-cache chunk attention on B300.
+
+One step = one streamed block of the 14B-DiT-shaped PR-Sink stream (40 heads
+x 128, 4680 tokens per block, static sink + top-2 pose-retrieved dynamic sink
++ 3-block window + current block = 32760 keys): pose retrieval and context
+selection, dynamic-sink fills from the caller's history store, 40 layers x 3
+denoising steps of chunk attention, and the 40 layer appends -- all through
+the library's C ABI (la_stream_step).  The stream is resumed late (pose
+history of ~3590 blocks loaded) so every timed block is at steady state.
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "chunk-attn TFLOP/s & streamed blocks/s at 14B-DiT shape; % of BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def args_():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None, help="override (testing only)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ workload
+def workload():
+    from synth import C3_14B
+    return C3_14B
+
+
+def attn_flops(sc, kv_len):
+    return 4.0 * sc.num_heads * sc.tokens_per_block * kv_len * sc.head_dim
+
+
+def workload_desc(sc, b0, n):
+    return {
+        "workload": (f"{sc.name}: PR-Sink chunk attention, {sc.num_layers} layers x {sc.n_steps} "
+                     f"denoising steps per block, {sc.num_heads} heads x {sc.head_dim}, "
+                     f"{sc.tokens_per_block} tokens/block ({sc.frames_per_block}x{sc.grid_h}x"
+                     f"{sc.grid_w}), static sink 1 + pose top-{sc.dyn_topk} + window {sc.window} + "
+                     f"current = {(sc.static_sink + sc.dyn_topk + sc.window + 1) * sc.tokens_per_block}"
+                     f" keys, bf16, external history; stream blocks {b0}..{b0 + n - 1} of "
+                     f"{sc.n_blocks}"),
+        "tokens_per_block": sc.tokens_per_block, "heads": sc.num_heads, "head_dim": sc.head_dim,
+        "layers": sc.num_layers, "denoise_steps": sc.n_steps, "dyn_topk": sc.dyn_topk,
+        "kv_len": (sc.static_sink + sc.dyn_topk + sc.window + 1) * sc.tokens_per_block,
+        "l2": "inputs larger than L2 (per call: 144 MB Q/K/V, 671 MB attended K/V; L2 126 MB)",
+    }
+
+
+# ------------------------------------------------------------------ oracle leg
+class OracleSample:
+    """A bounded sample of one steady-state call for the CPU oracle: n_heads
+    heads x n_rows query rows against the full 32760-key context.  Inputs are
+    generated once (not timed); run() times the oracle's computation."""
+
+    def __init__(self, sc, n_heads=8, n_rows=512):
+        from oracle import stream as ostream
+        from synth import gen
+        self.sc = sc
+        heads = list(np.linspace(0, sc.num_heads - 1, n_heads).astype(int))
+        T, H, D = sc.tokens_per_block, sc.num_heads, sc.head_dim
+        idx = (np.arange(T)[:, None, None] * H + np.asarray(heads)[None, :, None]) * D + \
+            np.arange(D)[None, None, :]
+        idx = idx.reshape(-1).astype(np.uint64)
+        b = 40
+        kps = gen.poses(sc, n_blocks=b + 1)
+        self.ctx = ostream.plan_stream(sc, kps, b + 1)[b]
+        self.vals = {}
+        for blk in self.ctx.blocks:
+            for w in ("k", "v") if blk != b else ("q", "k", "v"):
+                key = gen.qkv_key(sc, 0, blk, 0, w)
+                self.vals[(blk, w)] = gen.tensor_np(key, None, "bf16", index_map=idx).reshape(T, n_heads, D)
+        self.rows = np.linspace(0, T - 1, n_rows).astype(int)
+        self.flops = 4.0 * n_heads * n_rows * self.ctx.kv_len * D
+        self.text = (f"one steady-state {sc.name} call (block {b}, {self.ctx.kv_len} keys): "
+                     f"{n_heads} of {H} heads x {n_rows} of {T} query rows, fp64 NumPy incl. "
+                     f"RoPE of the whole context; input generation not timed")
+
+    def run(self):
+        from oracle import stream as ostream
+        b = self.ctx.block
+        t0 = time.perf_counter()
+        ostream.chunk_attention(self.sc, self.ctx, self.vals[(b, "q")],
+                                lambda blk: (self.vals[(blk, "k")], self.vals[(blk, "v")]),
+                                rows=self.rows)
+        return time.perf_counter() - t0
+
+
+def run_reference(a):
+    """Reference arm: the CPU oracle as it stands, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    sc = workload()
+    smp = OracleSample(sc)
+    for _ in range(a.warmup):
+        smp.run()
+    times = [smp.run() for _ in range(a.steps)]
+    flops, text = smp.flops, smp.text
+    tot = sum(times)
+    value = flops * a.steps / tot / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": tot / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_desc(sc, smp.ctx.block, 1) | {"sample": text},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": text},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags) if f == "Active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(a):
+    import torch
+    import torch.distributed as dist
+    from bounded_kv_cache_la_b300 import build, capi
+    from synth import gen
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if not os.path.exists(capi.LIB_PATH):
+        build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    sc = workload()
+    if a.layers:
+        sc = sc.with_(num_layers=a.layers)
+    L, S, T, H, D = sc.num_layers, sc.n_steps, sc.tokens_per_block, sc.num_heads, sc.head_dim
+    n_run = a.warmup + a.steps
+    b0 = max(10, sc.n_blocks - n_run - 1)
+    kps = gen.poses(sc, n_blocks=sc.n_blocks + 1)
+
+    cfg = capi.config_for(sc, max_history=sc.n_blocks + 2)
+    cache = capi.Cache(cfg)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234 + rank)
+
+    def randn():
+        return torch.randn((T, H, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    # resident inputs: Q/K/V per (layer, step); outputs per layer
+    q = [[randn() for _ in range(S)] for _ in range(L)]
+    k = [[randn() for _ in range(S)] for _ in range(L)]
+    v = [[randn() for _ in range(S)] for _ in range(L)]
+    out = [torch.empty((T, H, D), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    # the caller's history store: block id -> bank entry (id mod 4), per layer
+    bank = [[(randn(), randn()) for _ in range(4)] for _ in range(L)]
+
+    cache.la_cache_load_history(kps[:b0].reshape(b0, 34))
+    for blk in [0] + list(range(b0 - sc.window, b0)):
+        for l in range(L):
+            kk, vv = bank[l][blk % 4]
+            cache.la_fill_window(l, blk, kk, vv)
+
+    qs = [q[l][s] for s in range(S) for l in range(L)]
+    ks = [k[l][s] for s in range(S) for l in range(L)]
+    vs = [v[l][s] for s in range(S) for l in range(L)]
+    os_ = [out[l] for s in range(S) for l in range(L)]
+    fills = {"n": 0}
+
+    def fill(layer, blk):
+        fills["n"] += 1
+        return bank[layer][blk % 4]
+
+    state = {"b": b0}
+
+    def step():
+        b = state["b"]
+        cache.la_stream_step(kps[b], S, qs, ks, vs, os_, fill=fill)
+        state["b"] = b + 1
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(a.warmup):
+        step()
+    barrier()
+    # per-attention-launch events over the timed region
+    n_attn = a.steps * S * L
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_attn)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_attn)]
+    for e in ev_s + ev_e:
+        e.record(stream)          # materialise the handles
+    torch.cuda.synchronize()
+    cache.la_set_profile_events([e.cuda_event for e in ev_s], [e.cuda_event for e in ev_e])
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    time.sleep(0.5)
+    fills0 = fills["n"]
+    launches0 = capi.la_launch_count()
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for _ in range(a.steps):
+        step()
+    t_end.record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    launches = capi.la_launch_count() - launches0
+    fills_timed = fills["n"] - fills0
+    cache.la_set_profile_events([], [])
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    attn_ms = np.array([s.elapsed_time(e) for s, e in zip(ev_s, ev_e)])
+    st, msg = cache.la_get_error()
+    if st != capi.LA_OK:
+        raise RuntimeError(msg)
+
+    ctx_kv = (sc.static_sink + sc.dyn_topk + sc.window + 1) * T
+    flops_call = attn_flops(sc, ctx_kv)
+    flops_block = flops_call * S * L
+    t = torch.tensor([elapsed], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t_max = float(t.item())
+    value = flops_block * a.steps * world / t_max / 1e12
+    blocks_per_s = a.steps * world / t_max
+
+    pk, pk_kind = peaks()
+    achieved = flops_call / (attn_ms.mean() / 1e3) / 1e12
+    peak_sus = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+
+    # end to end through the per-call C ABI with pinned host inputs/outputs
+    e2e = None
+    if not a.no_e2e:
+        hq = torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory()
+        hk = torch.empty_like(hq).pin_memory()
+        hv = torch.empty_like(hq).pin_memory()
+        ho = torch.empty_like(hq).pin_memory()
+        hq.copy_(q[0][0].cpu()); hk.copy_(k[0][0].cpu()); hv.copy_(v[0][0].cpu())
+        dq, dk, dv = torch.empty_like(q[0][0]), torch.empty_like(q[0][0]), torch.empty_like(q[0][0])
+        dk_last = [torch.empty_like(q[0][0]) for _ in range(L)]
+        dv_last = [torch.empty_like(q[0][0]) for _ in range(L)]
+        h2d = d2h = 0
+
+        def e2e_step():
+            nonlocal h2d, d2h
+            b = state["b"]
+            ctx = cache.la_select_context(kps[b])
+            for i, blk in enumerate(ctx["dyn_ids"]):
+                if ctx["need_fill"][i]:
+                    for l in range(L):
+                        kk, vv = bank[l][blk % 4]
+                        cache.la_fill_block(l, blk, kk, vv)
+            for s in range(S):
+                for l in range(L):
+                    last = s == S - 1
+                    kd = dk_last[l] if last else dk
+                    vd = dv_last[l] if last else dv
+                    dq.copy_(hq, non_blocking=True)
+                    kd.copy_(hk, non_blocking=True)
+                    vd.copy_(hv, non_blocking=True)
+                    h2d += 3 * hq.numel() * 2
+                    cache.la_chunk_attention(l, dq, kd, vd, out[l])
+                    ho.copy_(out[l], non_blocking=True)
+                    d2h += ho.numel() * 2
+            for l in range(L):
+                cache.la_cache_append_block(l, dk_last[l], dv_last[l])
+            state["b"] = b + 1
+
+        e2e_step()
+        barrier()
+        h2d = d2h = 0
+        e0 = time.perf_counter()
+        for _ in range(a.e2e_steps):
+            e2e_step()
+        barrier()
+        e_el = time.perf_counter() - e0
+        te = torch.tensor([e_el], device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": flops_block * a.e2e_steps * world / float(te.item()) / 1e12,
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d // a.e2e_steps,
+               "d2h_bytes_per_step": d2h // a.e2e_steps,
+               "blocks_per_s": a.e2e_steps * world / float(te.item()), "steps": a.e2e_steps,
+               "api": "la_select_context + la_fill_block + la_chunk_attention + "
+                      "la_cache_append_block, pinned host Q/K/V in and every output back"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        smp = OracleSample(workload())
+        dt = min(smp.run() for _ in range(2))
+        cpu = {"value": smp.flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+               "kind": "oracle", "sample": smp.text, "seconds": dt}
+
+    if rank == 0:
+        traffic = None
+        prof_path = os.path.join(ROOT, "profiles", "attn_tc_c3_14b.json")
+        if os.path.exists(prof_path):
+            traffic = json.load(open(prof_path)).get("traffic_bytes_per_launch")
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": t_max / a.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded torch.randn Q/K/V, synthetic pose stream)",
+            "config": workload_desc(sc, b0 + a.warmup, a.steps) | {"parallelism": f"replicas x{world}"},
+            "blocks_per_s": blocks_per_s,
+            "per_block_latency_ms": t_max / a.steps * 1e3,
+            "frac_of_bf16_peak": value / pk["bf16_tflops"],
+            "frac_of_bf16_peak_sustained": value / peak_sus,
+            "attn_call_ms": {"mean": float(attn_ms.mean()), "min": float(attn_ms.min()),
+                             "max": float(attn_ms.max()), "n": int(attn_ms.size)},
+            "fills_per_block": fills_timed / a.steps,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_sus,
+                         "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": traffic,
+                         "kernel": "attn_tc_kernel", "peak_kind": f"bf16 sustained, {pk_kind}",
+                         "frac_of_burst": achieved / pk["bf16_tflops"]},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "wall_s": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    a = args_()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

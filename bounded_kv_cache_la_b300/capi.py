@@ -27,7 +27,8 @@ EXPORTS = (
     "la_cache_required_bytes", "la_cache_create", "la_cache_destroy", "la_select_context",
     "la_fill_block", "la_chunk_attention", "la_cache_append_block", "la_stream_step",
     "la_cache_load_history", "la_fill_window", "la_get_error", "la_context_plan",
-    "la_debug_page", "la_debug_memory", "la_status_string",
+    "la_debug_page", "la_debug_memory", "la_set_profile_events", "la_launch_count",
+    "la_status_string",
 )
 
 
@@ -117,6 +118,8 @@ def load() -> ctypes.CDLL:
         "la_debug_page": (i32, [vp, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp)]),
         "la_debug_memory": (i32, [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                   ctypes.POINTER(vp), ctypes.POINTER(i32), ctypes.POINTER(i32)]),
+        "la_set_profile_events": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i32]),
+        "la_launch_count": (ctypes.c_uint64, []),
         "la_status_string": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -171,6 +174,10 @@ def _check(st: int, where: str, handle=None):
 
 def la_cache_required_bytes(cfg: la_cache_config) -> int:
     return load().la_cache_required_bytes(ctypes.byref(cfg))
+
+
+def la_launch_count() -> int:
+    return int(load().la_launch_count())
 
 
 def la_context_plan(cfg: la_cache_config, block: int, dyn_ids=()) -> dict:
@@ -302,6 +309,13 @@ class Cache:
                                         ctypes.byref(r), ctypes.byref(n), ctypes.byref(o)),
                "la_debug_memory")
         return k.value, v.value, r.value, n.value, o.value
+
+    def la_set_profile_events(self, starts, stops):
+        """starts/stops: sequences of raw cudaEvent_t handles (ints)."""
+        n = len(starts)
+        a = (ctypes.c_void_p * max(1, n))(*starts)
+        b = (ctypes.c_void_p * max(1, n))(*stops)
+        _check(self.lib.la_set_profile_events(self.h, a, b, n), "la_set_profile_events")
 
     def view(self, addr: int, nbytes: int):
         """uint8 view of `nbytes` of the pool starting at device address addr."""

@@ -205,6 +205,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
   } else {
     append_kernel<LA_F32><<<grid, 256, 0, s>>>(a);
   }
+  count_launches(a.dst_dtype == LA_E4M3 ? 2 : 1);
   return cudaGetLastError();
 }
 

@@ -160,6 +160,7 @@ cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t s) {
   if (a.D == 128) attn_simt_kernel<4><<<grid, 256, 0, s>>>(a);
   else if (a.D == 64) attn_simt_kernel<2><<<grid, 256, 0, s>>>(a);
   else return cudaErrorInvalidValue;
+  count_launches(1);
   return cudaGetLastError();
 }
 

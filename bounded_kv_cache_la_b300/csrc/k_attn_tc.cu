@@ -476,6 +476,7 @@ cudaError_t launch_qrot(const QrotArgs& a, cudaStream_t s) {
   long long grid = (work + 255) / 256;
   if (grid > 148LL * 16) grid = 148LL * 16;
   qrot_kernel<<<(int)grid, 256, 0, s>>>(a);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -491,6 +492,7 @@ cudaError_t launch_attn_tc(const TcAttnArgs& a, int num_sms, cudaStream_t s) {
   const int units = a.H * n_pairs;
   const int grid = units < num_sms ? units : num_sms;
   attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -112,6 +112,7 @@ cudaError_t launch_convkv(const ConvArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   long long rot_work = (long long)a.H * a.n_after * (a.D / 8);
   rotate_ring_kernel<<<grid_for(rot_work), 256, 0, s>>>(a);
+  count_launches(2);
   return cudaGetLastError();
 }
 

@@ -24,6 +24,7 @@ cudaError_t launch_init_tables(float2* tab_t, int max_t, int dt, float2* tab_h, 
     int n = pt.rows * (pt.d / 2);
     if (n <= 0) continue;
     init_axis_table<<<(n + 255) / 256, 256, 0, s>>>(pt.p, pt.rows, pt.d, theta);
+    count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

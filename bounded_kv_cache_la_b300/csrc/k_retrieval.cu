@@ -152,6 +152,7 @@ cudaError_t launch_retrieval(const RetrievalArgs& a, cudaStream_t s) {
   int n = a.c1 > a.c0 ? a.c1 - a.c0 : 0;
   int grid = n > 0 ? (n + kCandPerCta - 1) / kCandPerCta : 1;
   retrieval_kernel<<<grid, kThreads, 0, s>>>(a);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -13,6 +13,7 @@
 // the per-block slot table is uploaded once per block and read by every
 // attention launch of that block.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -52,7 +53,14 @@ struct la_cache {
   bool tc = false;
   CUtensorMap tm_q{}, tm_kv{}, tm_cur{}, tm_mem{};
   int num_sms = 148;
+  std::vector<cudaEvent_t> prof_start, prof_stop;
+  size_t prof_next = 0;
 };
+
+namespace la {
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace la
 
 namespace {
 
@@ -398,6 +406,10 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
   if (st == LA_OK && cfg->kv_dtype == LA_E4M3)
     st = cuda_status(c, cudaMemsetAsync(c->pool + L.scales, 0, L.frames - L.scales, s),
                      "scale init");
+  // ConvKV rings start zeroed: attention reads whole tiles, so ring rows
+  // past the valid count must hold finite values (they get weight 0).
+  if (st == LA_OK && !is_prsink(*cfg))
+    st = cuda_status(c, cudaMemsetAsync(c->pool + L.mem, 0, L.total - L.mem, s), "memory init");
   c->tc = tc_eligible(*cfg, L);
   if (st == LA_OK && c->tc) {
     const int H = cfg->num_heads, D = cfg->head_dim;
@@ -680,7 +692,11 @@ la_status la_chunk_attention(la_cache_t* c, int layer, const void* q, const void
     ta.mem_row0 = layer * 3 * g.num_heads;
     ta.scale_log2 = g.softmax_scale * 1.4426950408889634f;
     ta.err = err;
-    return cuda_status(c, launch_attn_tc(ta, c->num_sms, s), "tensor-core attention");
+    const bool prof = c->prof_next < c->prof_start.size();
+    if (prof) cudaEventRecord(c->prof_start[c->prof_next], s);
+    st = cuda_status(c, launch_attn_tc(ta, c->num_sms, s), "tensor-core attention");
+    if (prof) cudaEventRecord(c->prof_stop[c->prof_next++], s);
+    return st;
   }
   AttnArgs a{};
   a.q = q;
@@ -705,7 +721,11 @@ la_status la_chunk_attention(la_cache_t* c, int layer, const void* q, const void
   a.scale = g.softmax_scale;
   a.rope = c->rope;
   a.err = err;
-  return cuda_status(c, launch_attn_simt(a, s), "simt attention");
+  const bool prof = c->prof_next < c->prof_start.size();
+  if (prof) cudaEventRecord(c->prof_start[c->prof_next], s);
+  st = cuda_status(c, launch_attn_simt(a, s), "simt attention");
+  if (prof) cudaEventRecord(c->prof_stop[c->prof_next++], s);
+  return st;
 }
 
 la_status la_cache_append_block(la_cache_t* c, int layer, const void* k, const void* v,
@@ -878,6 +898,20 @@ la_status la_debug_page(la_cache_t* c, int layer, int block_id, int which, void*
                                                       : nullptr;
   return LA_OK;
 }
+
+la_status la_set_profile_events(la_cache_t* c, void* const* starts, void* const* stops, int n) {
+  if (!c || n < 0 || (n > 0 && (!starts || !stops))) return LA_ERR_INVALID_ARG;
+  c->prof_start.assign(n, nullptr);
+  c->prof_stop.assign(n, nullptr);
+  for (int i = 0; i < n; ++i) {
+    c->prof_start[i] = static_cast<cudaEvent_t>(starts[i]);
+    c->prof_stop[i] = static_cast<cudaEvent_t>(stops[i]);
+  }
+  c->prof_next = 0;
+  return LA_OK;
+}
+
+uint64_t la_launch_count(void) { return la::g_launches.load(std::memory_order_relaxed); }
 
 la_status la_debug_memory(la_cache_t* c, int layer, void** k_raw, void** v, void** k_rot,
                           int* n_tokens, int* oldest) {

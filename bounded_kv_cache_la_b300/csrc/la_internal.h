@@ -83,6 +83,9 @@ struct RopeDims {
   const float2* tab_w;             // [GW][dw/2]
 };
 
+// Kernel launches enqueued by the library (every launcher adds its count).
+void count_launches(int n);
+
 // ------------------------------------------------------------ kernel launches
 // Each returns the cudaError_t of its launch(es).
 cudaError_t launch_init_tables(float2* tab_t, int max_t, int dt, float2* tab_h, int GH, int dh,

@@ -209,6 +209,16 @@ la_status la_debug_page(la_cache_t* cache, int layer, int block_id, int which,
 la_status la_debug_memory(la_cache_t* cache, int layer, void** k_raw, void** v, void** k_rot,
                           int* n_tokens, int* oldest);
 
+/* Profiling: `starts`/`stops` (host arrays of n cudaEvent_t, created by the
+ * caller) -- the i-th attention kernel launched after this call records
+ * starts[i] immediately before and stops[i] immediately after itself on the
+ * caller's stream, for i < n; later launches record nothing.  n = 0 turns
+ * recording off.  The arrays are copied; the events stay the caller's. */
+la_status la_set_profile_events(la_cache_t* cache, void* const* starts, void* const* stops, int n);
+
+/* Number of kernels this library has enqueued since it was loaded. */
+uint64_t la_launch_count(void);
+
 const char* la_status_string(la_status s);
 
 #ifdef __cplusplus

@@ -209,9 +209,10 @@ def run_ours(a):
     if a.layers:
         sc = sc.with_(num_layers=a.layers)
     L, S, T, H, D = sc.num_layers, sc.n_steps, sc.tokens_per_block, sc.num_heads, sc.head_dim
-    n_run = a.warmup + a.steps
-    b0 = max(10, sc.n_blocks - n_run - 1)
-    kps = gen.poses(sc, n_blocks=sc.n_blocks + 1)
+    # blocks streamed: warm-up, timed, and (e2e leg) one warm-up + e2e_steps
+    n_run = a.warmup + a.steps + (0 if a.no_e2e else a.e2e_steps + 1)
+    b0 = max(10, sc.n_blocks - n_run)
+    kps = gen.poses(sc, n_blocks=b0 + n_run + 1)
 
     cfg = capi.config_for(sc, max_history=sc.n_blocks + 2)
     cache = capi.Cache(cfg)
@@ -283,10 +284,12 @@ def run_ours(a):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     wall0 = time.perf_counter()
+    torch.cuda.nvtx.range_push("timed")
     t_start.record(stream)
     for _ in range(a.steps):
         step()
     t_end.record(stream)
+    torch.cuda.nvtx.range_pop()
     barrier()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()

@@ -19,6 +19,7 @@ LA_F32, LA_BF16, LA_E4M3 = 0, 1, 2
 LA_HISTORY_RESIDENT, LA_HISTORY_EXTERNAL = 0, 1
 LA_ATTN_AUTO, LA_ATTN_TENSOR, LA_ATTN_SIMT = 0, 1, 2
 LA_MAX_SLOTS, LA_MAX_TOPK = 16, 8
+LA_NOALLOC_MAX_ROWS = 65536
 
 DTYPES = {"f32": LA_F32, "bf16": LA_BF16, "e4m3": LA_E4M3}
 
@@ -28,7 +29,7 @@ EXPORTS = (
     "la_fill_block", "la_chunk_attention", "la_cache_append_block", "la_stream_step",
     "la_cache_load_history", "la_fill_window", "la_get_error", "la_context_plan",
     "la_debug_page", "la_debug_memory", "la_set_profile_events", "la_launch_count",
-    "la_status_string",
+    "la_status_string", "la_pose_topk_noalloc",
 )
 
 
@@ -121,6 +122,8 @@ def load() -> ctypes.CDLL:
         "la_set_profile_events": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i32]),
         "la_launch_count": (ctypes.c_uint64, []),
         "la_status_string": (ctypes.c_char_p, [i32]),
+        "la_pose_topk_noalloc": (i32, [vp, vp, i32, ctypes.POINTER(ctypes.c_float), i32, i32, i32,
+                                       i32, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -187,6 +190,22 @@ def la_context_plan(cfg: la_cache_config, block: int, dyn_ids=()) -> dict:
     _check(lib.la_context_plan(ctypes.byref(cfg), block, arr, len(dyn_ids), ctypes.byref(out)),
            "la_context_plan")
     return out.as_dict()
+
+
+def la_pose_topk_noalloc(table, inv_norm, query_kp, pose_row, c0, c1, k, ids_out, scores_out,
+                         n_out, stream=None):
+    """Pose top-k with the library's fixed scratch (no device allocation).
+
+    table [max_rows, 36] and inv_norm [max_rows] are caller-owned float32
+    device tensors; ids_out (int32), scores_out (float32) hold k + 1 entries
+    and n_out (int32) one, all on the device.  query_kp: host, 17 x 2."""
+    import numpy as np
+    kp = np.ascontiguousarray(np.asarray(query_kp, dtype=np.float32).reshape(34))
+    _check(load().la_pose_topk_noalloc(
+        _ptr(table), _ptr(inv_norm), int(table.shape[0]),
+        kp.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), pose_row, c0, c1, k,
+        _ptr(ids_out), _ptr(scores_out), _ptr(n_out), _stream_handle(stream)),
+        "la_pose_topk_noalloc")
 
 
 def _stream_handle(stream) -> ctypes.c_void_p:

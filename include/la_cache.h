@@ -221,6 +221,50 @@ uint64_t la_launch_count(void);
 
 const char* la_status_string(la_status s);
 
+/* Pose top-k without any device allocation (the pages have no counterpart:
+ * this call exists for callers, not for the method).
+ *
+ * Some callers cannot call cudaMalloc at the moment they need a retrieval:
+ * a host that hands out only pre-sized buffers and forbids allocation once
+ * serving has started, or code on a real-time path where an allocation's
+ * implicit device synchronisation would stall the stream.  la_select_context
+ * keeps its retrieval scratch in the cache pool, which needs a created
+ * cache.  This call runs the same retrieval kernel with its scratch (the
+ * per-candidate scores, the top-k state and an error word) in one fixed
+ * array inside the library: `static __device__`, LA_NOALLOC_MAX_ROWS scores
+ * (256 KB + 256 B), held by every GPU that loads the library until the
+ * process exits.
+ *
+ * table    device, [max_rows][36] fp32, caller-owned, 16-byte aligned: row j
+ *          is block j's centred descriptor (x0, y0, ..., x16, y16, 0, 0);
+ * inv_norm device, [max_rows] fp32, caller-owned: 1/|descriptor| (0 if zero);
+ *          rows are written by this call itself when pose_row >= 0, so a
+ *          caller builds its history by calling once per block;
+ * query_kp host, 17 (x, y) keypoints of the block being generated;
+ * pose_row table row that receives the query's descriptor, or -1 for none;
+ * [c0, c1) candidate block ids scored against the query (rows already
+ *          written); 0 <= c0 <= c1 <= min(max_rows, LA_NOALLOC_MAX_ROWS);
+ * k        0 .. LA_MAX_TOPK picks; k + 1 entries are ranked so that the gap
+ *          score_k - score_(k+1) can be read;
+ * ids_out, scores_out  device, k + 1 entries each, in rank order (score
+ *          descending, id ascending); n_out device, 1 int32: entries ranked.
+ *
+ * Sizes beyond the scratch (c1 > LA_NOALLOC_MAX_ROWS) are rejected with
+ * LA_ERR_INVALID_ARG before any work is enqueued, as are bad pointers and
+ * ranges.  The call enqueues a memset of the scratch header, the kernel and
+ * three device-to-device copies on `stream`, and does not synchronise.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine.  Its first
+ * call on a device (with that device current) looks up the scratch array's
+ * device address; make that first call before any stream capture.  Every
+ * call shares the one array and it keeps the last call's contents: calls
+ * that overlap on the GPU (different streams, no ordering) race and give
+ * wrong results. */
+#define LA_NOALLOC_MAX_ROWS 65536
+la_status la_pose_topk_noalloc(float* table, float* inv_norm, int max_rows,
+                               const float* query_kp, int pose_row, int c0, int c1, int k,
+                               int32_t* ids_out, float* scores_out, int32_t* n_out,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif

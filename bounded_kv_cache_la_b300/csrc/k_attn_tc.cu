@@ -15,8 +15,14 @@
 // slot table says which page), 128 keys x 64 dims per box, 128-byte swizzle;
 // rows past a slot's end are zero-filled by TMA and masked to -inf.
 //
-// CTA = 2 query tiles of 128 rows of one head, persistent over (head, tile
-// pair) units.  12 warps:
+// Work units.  A unit is (head, pair of 128-row query tiles).  When a head
+// has an odd number of query tiles its last unit is a half unit (one tile).
+// Units are ordered full units first, half units last, and dealt to the
+// persistent CTAs in a snake order (CTA c takes index i*G + c on even rounds
+// and i*G + G-1-c on odd rounds), so that the CTAs that get an extra half
+// unit are the ones that got fewer full units.
+//
+// CTA = 12 warps, persistent:
 //   warp 0       TMA producer (K ring, V ring, per-slot Q tiles)
 //   warp 1       MMA issuer: S_i = Q_i K^T (smem x smem) into TMEM,
 //                O_i += P_i V (P from TMEM, V from smem, MN-major)
@@ -25,9 +31,18 @@
 //   warps 8..11  softmax of query tile 1
 // TMEM columns: S0 | S1 | O0 | O1 (128 each); P_i overwrites S_i as bf16.
 // Issue order PV0(j-1), QK0(j), PV1(j-1), QK1(j) lets each softmax run while
-// the tensor core works on the other tile.  Online softmax in base 2 with a
-// lazy rescale: the running max moves only when a row's max grows by more
-// than 8 (a factor 256), then O and l are rescaled in TMEM / registers.
+// the tensor core works on the other tile.
+//
+// Softmax.  Base-2 online softmax with a lazy rescale: the running max moves
+// only when a row's max grows by more than 8 (a factor 256), then O and l are
+// rescaled.  The row max is a tree of 3-input maxes; scale-and-subtract and
+// the row sum use packed fp32x2 arithmetic.  The exponentials are split
+// between the MUFU unit (ex2.approx) and the FMA pipe as a build option:
+// kEmuPairs of every 16 column pairs use 2^x = 2^n * p(x - n), n = rint(x) (Cody and Waite's
+// reduction, exact in base 2), p a degree-3 minimax polynomial for 2^f on
+// [-1/2, 1/2] (max relative error 7.5e-5, fitted by csrc/fit_exp2_poly.py),
+// and 2^n added to the exponent bits.  P is rounded to bf16 (relative error
+// 2^-9) before the PV product either way.
 //
 // Every wait is bounded (2 s); on timeout the kernel latches LA_ERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and returns.
@@ -55,12 +70,24 @@ constexpr int kCtlBytes = 1024;
 constexpr int kSmemBytes = kOffCtl + kCtlBytes + 1024;   // + alignment slack
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 // Register split: launched at 168 per thread (384 threads, 1 CTA per SM =
-// 64512).  Control warpgroup 128 x 72 + two softmax warpgroups 2 x 128 x 208
-// = 62464 <= 64512.
-constexpr int kRegsCtl = 72;
+// 64512).  Control warpgroup 128 x 88 + two softmax warpgroups 2 x 128 x 208
+// = 64512.
+constexpr int kRegsCtl = 88;
 constexpr int kRegsSoftmax = 208;
 static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * 168, "register split too large");
 constexpr float kRescaleThreshold = 8.0f;                 // log2(256)
+// Measured at the 14B shape (one call, B300): 0 -> 2.75 ms, 4 -> 2.91,
+// 6 -> 2.98, 8 -> 3.08: the exponentials are not the binding unit here, so
+// the default keeps them all on MUFU.
+#ifndef LA_EMU_PAIRS
+#define LA_EMU_PAIRS 0
+#endif
+constexpr int kEmuPairs = LA_EMU_PAIRS;                   // of every 16 column pairs
+static_assert(kEmuPairs >= 0 && kEmuPairs <= 16, "kEmuPairs out of range");
+
+// 2^f on [-1/2, 1/2]: c0 + c1 f + c2 f^2 + c3 f^3 (fp32 bit patterns).
+constexpr uint32_t kP0 = 0x3f7ffb49u, kP1 = 0x3f31798du, kP2 = 0x3e786f0du, kP3 = 0x3d61fbb0u;
+constexpr float kRoundMagic = 12582912.0f;                // 1.5 * 2^23
 
 struct Ctl {
   uint64_t q_full, q_empty;
@@ -95,6 +122,34 @@ struct Wait {
   }
 };
 
+// Work units: full (head, tile pair) units first, then one half unit per
+// head when the head has an odd number of query tiles.
+struct Units {
+  int H, n_full, n_units;
+  __device__ Units(int T, int H_) : H(H_) {
+    const int nt_q = (T + kBM - 1) / kBM;
+    n_full = nt_q / 2;
+    n_units = H * n_full + ((nt_q & 1) ? H : 0);
+  }
+  // CTA c's i-th unit index in snake order (may be >= n_units: done).
+  __device__ __forceinline__ int index(int i) const {
+    const int G = gridDim.x, c = blockIdx.x;
+    return i * G + ((i & 1) ? (G - 1 - c) : c);
+  }
+  __device__ __forceinline__ void get(int u, int& h, int& row0, bool& half) const {
+    const int nf = H * n_full;
+    if (u < nf) {
+      h = u / n_full;
+      row0 = (u - h * n_full) * 2 * kBM;
+      half = false;
+    } else {
+      h = u - nf;
+      row0 = n_full * 2 * kBM;
+      half = true;
+    }
+  }
+};
+
 // Tensor map and row of slot s's key (which = 0) or value (which = 1) pages.
 __device__ __forceinline__ const CUtensorMap* kv_map(const TcAttnArgs& a, const DevContext& c, int s,
                                                      int which, int h, int& row) {
@@ -109,6 +164,24 @@ __device__ __forceinline__ const CUtensorMap* kv_map(const TcAttnArgs& a, const 
   }
   row = a.mem_row0 + (which == 0 ? 2 : 1) * a.H + h;     // rotated-key ring / value ring
   return &a.tm_mem;
+}
+
+// 2^x for a pair on the FMA pipe (x <= 2^7; x below -125 gives 2^-125-ish,
+// negligible next to the row max's 1).
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  x.x = fmaxf(x.x, -125.f);
+  x.y = fmaxf(x.y, -125.f);
+  const float2 t = fadd2(x, make_float2(kRoundMagic, kRoundMagic));      // rint(x) in the low bits
+  const float2 n = fsub2(t, make_float2(kRoundMagic, kRoundMagic));
+  const float2 f = fsub2(x, n);                                          // exact, |f| <= 1/2
+  const float2 c3 = make_float2(__uint_as_float(kP3), __uint_as_float(kP3));
+  const float2 c2 = make_float2(__uint_as_float(kP2), __uint_as_float(kP2));
+  const float2 c1 = make_float2(__uint_as_float(kP1), __uint_as_float(kP1));
+  const float2 c0 = make_float2(__uint_as_float(kP0), __uint_as_float(kP0));
+  float2 p = ffma2(ffma2(ffma2(c3, f, c2), f, c1), f, c0);
+  p.x = __int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23));
+  p.y = __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23));
+  return p;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcAttnArgs a) {
@@ -164,8 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   }
   const Wait wait{&ctl.abort_flag, a.err};
   const uint32_t tmem = ctl.tmem_base;
-  const int n_pairs = (a.T + 2 * kBM - 1) / (2 * kBM);
-  const int n_units = a.H * n_pairs;
+  const Units units(a.T, a.H);
   if (bad && tid == 0) record_error(a.err, LA_ERR_DEVICE, KID_ATTN_TC, n_slots, -1);
 
   if (warp < 4) {
@@ -176,8 +248,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (lane == 0) {
       uint32_t kc = 0, vc = 0, qc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const int h = u / n_pairs, row0 = (u % n_pairs) * 2 * kBM;
+      for (int i = 0; ok; ++i) {
+        const int u = units.index(i);
+        if (u >= units.n_units) break;
+        int h, row0;
+        bool half;
+        units.get(u, h, row0, half);
+        const int n_qt = half ? 1 : 2;
         for (int s = 0; ok && s < n_slots; ++s) {
           const int nt = (cx.tokens[s] + kBN - 1) / kBN;
           int krow, vrow;
@@ -193,11 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             ++kc;
             if (kt == 0) {
               if (!(ok = wait(ctl.q_empty, (qc & 1) ^ 1, 2))) break;
-              mbar_arrive_expect_tx(smem_u32(&ctl.q_full), 2 * kTileBytes);
-              for (int i = 0; i < 2; ++i)
+              mbar_arrive_expect_tx(smem_u32(&ctl.q_full), n_qt * kTileBytes);
+              for (int qi = 0; qi < n_qt; ++qi)
                 for (int hf = 0; hf < 2; ++hf)
-                  tma_load_3d(sQ + i * kTileBytes + hf * kHalfBytes, &a.tm_q, hf * 64,
-                              row0 + i * kBM, s * a.H + h, smem_u32(&ctl.q_full));
+                  tma_load_3d(sQ + qi * kTileBytes + hf * kHalfBytes, &a.tm_q, hf * 64,
+                              row0 + qi * kBM, s * a.H + h, smem_u32(&ctl.q_full));
               ++qc;
             }
             const int vs = vc % kVSt;
@@ -232,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16(kBM, kBN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(kBM, kD, 0, 1);
-      uint32_t kc = 0, vc = 0, qc = 0, pc = 0;
+      uint32_t kc = 0, vc = 0, qc = 0, pc0 = 0, pc1 = 0;
       bool ok = true;
       auto issue_qk = [&](int i, int ks) {
         const uint32_t q = sQ + i * kTileBytes, k = sK + ks * kTileBytes;
@@ -249,7 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, sdesc(v + kk * 2048, kHalfBytes, 1024), idesc_pv,
                  !(first && kk == 0));
       };
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+      for (int i = 0; ok; ++i) {
+        const int u = units.index(i);
+        if (u >= units.n_units) break;
+        int h, row0;
+        bool half;
+        units.get(u, h, row0, half);
         int j = 0;
         for (int s = 0; ok && s < n_slots; ++s) {
           const int nt = (cx.tokens[s] + kBN - 1) / kBN;
@@ -259,10 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             tc_fence_after();
             const int vs = vc % kVSt;
             if (j > 0) {
-              if (!(ok = wait(ctl.p_ready[0], pc & 1, 12))) break;
+              if (!(ok = wait(ctl.p_ready[0], pc0 & 1, 12))) break;
               if (!(ok = wait(ctl.v_full[vs], (vc / kVSt) & 1, 13))) break;
               tc_fence_after();
               issue_pv(0, vs, j == 1);
+              ++pc0;
             }
             if (kt == 0) {
               if (!(ok = wait(ctl.q_full, qc & 1, 14))) break;
@@ -272,15 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             issue_qk(0, ks);
             tc_commit(smem_u32(&ctl.s_full[0]));
             if (j > 0) {
-              if (!(ok = wait(ctl.p_ready[1], pc & 1, 15))) break;
-              tc_fence_after();
-              issue_pv(1, vs, j == 1);
+              if (!half) {
+                if (!(ok = wait(ctl.p_ready[1], pc1 & 1, 15))) break;
+                tc_fence_after();
+                issue_pv(1, vs, j == 1);
+                ++pc1;
+              }
               tc_commit(smem_u32(&ctl.v_empty[vs]));
               ++vc;
-              ++pc;
             }
-            issue_qk(1, ks);
-            tc_commit(smem_u32(&ctl.s_full[1]));
+            if (!half) {
+              issue_qk(1, ks);
+              tc_commit(smem_u32(&ctl.s_full[1]));
+            }
             tc_commit(smem_u32(&ctl.k_empty[ks]));
             ++kc;
             if (kt == nt - 1) tc_commit(smem_u32(&ctl.q_empty));
@@ -289,18 +376,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (!ok) break;
         // last tile of the unit
         const int vs = vc % kVSt;
-        if (!(ok = wait(ctl.p_ready[0], pc & 1, 16))) break;
+        if (!(ok = wait(ctl.p_ready[0], pc0 & 1, 16))) break;
         if (!(ok = wait(ctl.v_full[vs], (vc / kVSt) & 1, 17))) break;
         tc_fence_after();
         issue_pv(0, vs, j == 1);
+        ++pc0;
         tc_commit(smem_u32(&ctl.o_full[0]));
-        if (!(ok = wait(ctl.p_ready[1], pc & 1, 18))) break;
-        tc_fence_after();
-        issue_pv(1, vs, j == 1);
-        tc_commit(smem_u32(&ctl.o_full[1]));
+        if (!half) {
+          if (!(ok = wait(ctl.p_ready[1], pc1 & 1, 18))) break;
+          tc_fence_after();
+          issue_pv(1, vs, j == 1);
+          ++pc1;
+          tc_commit(smem_u32(&ctl.o_full[1]));
+        }
         tc_commit(smem_u32(&ctl.v_empty[vs]));
         ++vc;
-        ++pc;
       }
       // every MMA issued has completed before TMEM is released
       tc_commit(smem_u32(&ctl.mma_done));
@@ -312,24 +402,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
    setmaxnreg_inc<kRegsSoftmax>();
    if (!bad) {
     // ------------------------------------------------------------ softmax
-    const int i = (warp - 4) >> 2;                 // query tile of this warpgroup
+    const int qi = (warp - 4) >> 2;                // query tile of this warpgroup
     const int quad = warp & 3;                     // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;                // row within the tile
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + i * 128;
-    const uint32_t tO = tmem + lane_off + 256 + i * 128;
+    const uint32_t tS = tmem + lane_off + qi * 128;
+    const uint32_t tO = tmem + lane_off + 256 + qi * 128;
     const float c = a.scale_log2;
     uint32_t sph = 0, oph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-      const int h = u / n_pairs, row0 = (u % n_pairs) * 2 * kBM;
+    for (int i = 0; ok; ++i) {
+      const int u = units.index(i);
+      if (u >= units.n_units) break;
+      int h, row0;
+      bool half;
+      units.get(u, h, row0, half);
+      if (half && qi == 1) continue;               // the tile past the head's last rows
       float m = -INFINITY, l = 0.f;
       int j = 0;
       for (int s = 0; ok && s < n_slots; ++s) {
         const int tokens = cx.tokens[s];
         const int nt = (tokens + kBN - 1) / kBN;
         for (int kt = 0; kt < nt; ++kt, ++j) {
-          ok = __all_sync(0xffffffffu, wait(ctl.s_full[i], sph & 1, 21 + i));
+          ok = __all_sync(0xffffffffu, wait(ctl.s_full[qi], sph & 1, 21 + qi));
           if (!ok) break;
           ++sph;
           tc_fence_after();
@@ -343,9 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             for (int cc = 0; cc < kBN; ++cc)
               if (cc >= valid) sv[cc] = -INFINITY;
           }
-          float mx = sv[0];
+          // row max: 8 independent 3-input max chains, then a tree
+          float t8[8];
 #pragma unroll
-          for (int cc = 1; cc < kBN; ++cc) mx = fmaxf(mx, sv[cc]);
+          for (int e = 0; e < 8; ++e) t8[e] = fmax3(sv[e], sv[e + 8], sv[e + 16]);
+#pragma unroll
+          for (int b = 24; b + 16 <= kBN; b += 16)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t8[e] = fmax3(t8[e], sv[b + e], sv[b + 8 + e]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t8[e] = fmaxf(t8[e], sv[kBN - 8 + e]);
+          float mx = fmaxf(fmax3(t8[0], t8[1], t8[2]), fmax3(fmax3(t8[3], t8[4], t8[5]), t8[6], t8[7]));
           mx *= c;
           if (__any_sync(0xffffffffu, mx > m + kRescaleThreshold)) {
             const float m_new = fmaxf(m, mx);
@@ -365,32 +468,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             l *= alpha;
             m = m_new;
           }
-          float sum = 0.f;
+          const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
+          for (int hf = 0; hf < 2; ++hf) {
             uint32_t pk[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const float p0 = ex2(fmaf(sv[half * 64 + 2 * e], c, -m));
-              const float p1 = ex2(fmaf(sv[half * 64 + 2 * e + 1], c, -m));
-              sum += p0 + p1;
-              pk[e] = pack_bf16x2(p0, p1);
+              const float2 x = ffma2(make_float2(sv[hf * 64 + 2 * e], sv[hf * 64 + 2 * e + 1]), c2, nm2);
+              float2 p;
+              if ((e & 15) < kEmuPairs) {
+                p = exp2_poly2(x);
+              } else {
+                p.x = ex2(x.x);
+                p.y = ex2(x.y);
+              }
+              acc[e & 3] = fadd2(acc[e & 3], p);
+              pk[e] = cvt_bf16x2(p.x, p.y);
             }
-            tmem_st32(tS + half * 32, pk);
+            tmem_st32(tS + hf * 32, pk);
           }
-          l += sum;
+          const float2 s01 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+          l += s01.x + s01.y;
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(smem_u32(&ctl.p_ready[i]));
+          mbar_arrive(smem_u32(&ctl.p_ready[qi]));
         }
       }
       if (!ok) break;
-      ok = __all_sync(0xffffffffu, wait(ctl.o_full[i], oph & 1, 23 + i));
+      ok = __all_sync(0xffffffffu, wait(ctl.o_full[qi], oph & 1, 23 + qi));
       if (!ok) break;
       ++oph;
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const int row = row0 + i * kBM + r;
+      const int row = row0 + qi * kBM + r;
       uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + ((size_t)row * a.H + h) * kD;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -400,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          pk[e] = cvt_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
         if (row < a.T) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll

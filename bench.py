@@ -47,6 +47,8 @@ def args_():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the FP8, ConvKV and latency-flatness legs")
     ap.add_argument("--layers", type=int, default=None, help="override (testing only)")
     return ap.parse_args()
 
@@ -187,6 +189,159 @@ class ClockSampler:
                 "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ extra legs
+def fp8_peak_tflops(torch):
+    """Dense e4m3 GEMM throughput of this GPU (torch._scaled_mm, 8192^3,
+    best of 10, CUDA events): the denominator of the FP8 fractions."""
+    try:
+        n = 8192
+        a = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn)
+        one = torch.ones((), device="cuda")
+        f = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            f()
+        best = None
+        for _ in range(10):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(); f(); e.record(); e.synchronize()
+            t = s.elapsed_time(e) / 1e3
+            best = t if best is None else min(best, t)
+        return 2.0 * n ** 3 / best / 1e12
+    except Exception as exc:                    # noqa: BLE001
+        return {"unavailable": str(exc)[:200]}
+
+
+class StreamLeg:
+    """One stream of a workload driven block by block through la_stream_step.
+
+    External-history streams resume at block b0 (pose history loaded, sink
+    and window supplied from the bank); resident / ConvKV streams are run
+    from block 0 to b0 untimed.  Q/K/V cycle through `n_sets` resident sets
+    (larger than L2 together)."""
+
+    def __init__(self, torch, capi, gen, sc, b0, n_after, q, k, v, out, bank):
+        self.torch, self.capi, self.sc = torch, capi, sc
+        L, S = sc.num_layers, sc.n_steps
+        self.kps = gen.poses(sc, n_blocks=b0 + n_after + 1)
+        conv_w = None
+        if sc.policy == "convkv":
+            conv_w = torch.stack([gen.conv_weights_torch(sc, l, "cuda") for l in range(L)]).contiguous()
+        self.cache = capi.Cache(capi.config_for(sc, max_history=b0 + n_after + 2), conv_w=conv_w)
+        self.q, self.k, self.v, self.out, self.bank = q, k, v, out, bank
+        self.b = 0
+        if sc.history_mode == "external" and b0 > 0:
+            self.cache.la_cache_load_history(self.kps[:b0].reshape(b0, 34))
+            for blk in [0] + list(range(max(1, b0 - sc.window), b0)):
+                for l in range(L):
+                    self.cache.la_fill_window(l, blk, *bank[l % len(bank)][blk % 4])
+            self.b = b0
+        while self.b < b0:
+            self.step()
+
+    def step(self):
+        sc, L, S = self.sc, self.sc.num_layers, self.sc.n_steps
+        n = len(self.q)
+        i = self.b % n
+        qs = [self.q[(i + l) % n] for s in range(S) for l in range(L)]
+        ks = [self.k[(i + l + s) % n] for s in range(S) for l in range(L)]
+        vs = [self.v[(i + l + s) % n] for s in range(S) for l in range(L)]
+        os_ = [self.out[l % len(self.out)] for s in range(S) for l in range(L)]
+        bank = self.bank
+        self.cache.la_stream_step(self.kps[self.b], S, qs, ks, vs, os_,
+                                  fill=lambda layer, blk: bank[layer % len(bank)][blk % 4])
+        self.b += 1
+
+    def time_blocks(self, n_blocks):
+        """Per-block ms (CUDA events around each streamed block) and
+        per-attention-call ms (events around every attention launch)."""
+        torch = self.torch
+        L, S = self.sc.num_layers, self.sc.n_steps
+        n_attn = n_blocks * L * S
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_attn + n_blocks + 1)]
+        for e in ev:
+            e.record()
+        torch.cuda.synchronize()
+        a_s, a_e, blk = ev[:n_attn], ev[n_attn:2 * n_attn], ev[2 * n_attn:]
+        self.cache.la_set_profile_events([e.cuda_event for e in a_s], [e.cuda_event for e in a_e])
+        blk[0].record()
+        for i in range(n_blocks):
+            self.step()
+            blk[i + 1].record()
+        torch.cuda.synchronize()
+        self.cache.la_set_profile_events([], [])
+        st, msg = self.cache.la_get_error()
+        if st != self.capi.LA_OK:
+            raise RuntimeError(msg)
+        block_ms = [blk[i].elapsed_time(blk[i + 1]) for i in range(n_blocks)]
+        attn_ms = [s.elapsed_time(e) for s, e in zip(a_s, a_e)]
+        return block_ms, attn_ms
+
+    def close(self):
+        self.cache.close()
+
+
+def extra_legs(torch, capi, gen, q, k, v, out, bank, main_block_ms, pk):
+    """FP8 stress stream, ConvKV stream and the latency-flatness check."""
+    from synth import C3_14B, C4_CONVKV, C5_FP8
+    res = {}
+    fp8_pk = fp8_peak_tflops(torch)
+    # latency flatness of the 14B stream: blocks 10..12 against the timed blocks
+    leg = StreamLeg(torch, capi, gen, C3_14B, 10, 3, q, k, v, out, bank)
+    early, _ = leg.time_blocks(3)
+    leg.close()
+    res["flatness"] = {"c3_14b": {
+        "early_blocks": "10-12", "early_block_ms": float(np.median(early)),
+        "late_block_ms": float(np.median(main_block_ms)),
+        "late_over_early": float(np.median(main_block_ms) / np.median(early))}}
+    # FP8 stress: e4m3 K/V, top-4 over a 10000-block pose history
+    sc = C5_FP8
+    kv = (1 + sc.dyn_topk + sc.window + 1) * sc.tokens_per_block
+    fl = attn_flops(sc, kv)
+    fp8 = {"kv_len": kv, "flop_per_call": fl}
+    for name, b0 in (("early", 10), ("late", sc.n_blocks - 3)):
+        leg = StreamLeg(torch, capi, gen, sc, b0, 3, q, k, v, out, bank)
+        leg.step()                               # warm-up block
+        bms, ams = leg.time_blocks(2)
+        leg.close()
+        fp8[f"{name}_blocks"] = f"{b0 + 1}-{b0 + 2}"
+        fp8[f"{name}_block_ms"] = float(np.median(bms))
+        fp8[f"{name}_attn_call_ms"] = float(np.mean(ams))
+    fp8["late_over_early"] = fp8["late_block_ms"] / fp8["early_block_ms"]
+    t_fp8 = fl / (fp8["late_attn_call_ms"] / 1e3) / 1e12
+    fp8["attn_tflops"] = t_fp8
+    fp8["blocks_per_s"] = 1e3 / fp8["late_block_ms"]
+    fp8["fp8_peak_tflops"] = fp8_pk
+    if isinstance(fp8_pk, float):
+        fp8["frac_of_fp8_peak"] = t_fp8 / fp8_pk
+    fp8["frac_of_bf16_peak"] = t_fp8 / pk["bf16_tflops"]
+    res["flatness"]["c5_fp8"] = {"early_block_ms": fp8["early_block_ms"],
+                                 "late_block_ms": fp8["late_block_ms"],
+                                 "late_over_early": fp8["late_over_early"]}
+    # ConvKV: streamed from block 0; memory full (4096 tokens) from block 9
+    sc4 = C4_CONVKV
+    T4, H, D = sc4.tokens_per_block, sc4.num_heads, sc4.head_dim
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    mk = lambda: torch.randn((T4, H, D), generator=g, device="cuda").to(torch.bfloat16)
+    q4, k4, v4 = [mk() for _ in range(4)], [mk() for _ in range(4)], [mk() for _ in range(4)]
+    o4 = [torch.empty((T4, H, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    leg = StreamLeg(torch, capi, gen, sc4, 10, 3, q4, k4, v4, o4, [[(k4[0], v4[0])] * 4])
+    bms, ams = leg.time_blocks(3)
+    leg.close()
+    kv4 = sc4.mem_slots + (sc4.window + 1) * T4
+    fl4 = attn_flops(sc4, kv4)
+    res["variants"] = {
+        "c5_fp8": fp8,
+        "c4_convkv": {"kv_len": kv4, "blocks": "10-12", "block_ms": float(np.median(bms)),
+                      "blocks_per_s": 1e3 / float(np.median(bms)),
+                      "attn_call_ms": float(np.mean(ams)),
+                      "attn_tflops": fl4 / (np.mean(ams) / 1e3) / 1e12,
+                      "frac_of_bf16_peak": fl4 / (np.mean(ams) / 1e3) / 1e12 / pk["bf16_tflops"]},
+    }
+    return res
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(a):
     import torch
@@ -284,10 +439,13 @@ def run_ours(a):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     wall0 = time.perf_counter()
+    blk_ev = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps - 1)]
     torch.cuda.nvtx.range_push("timed")
     t_start.record(stream)
-    for _ in range(a.steps):
+    for i in range(a.steps):
         step()
+        if i < a.steps - 1:
+            blk_ev[i].record(stream)
     t_end.record(stream)
     torch.cuda.nvtx.range_pop()
     barrier()
@@ -297,6 +455,8 @@ def run_ours(a):
     fills_timed = fills["n"] - fills0
     cache.la_set_profile_events([], [])
     elapsed = t_start.elapsed_time(t_end) / 1e3
+    marks = [t_start] + blk_ev + [t_end]
+    block_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(a.steps)]
     attn_ms = np.array([s.elapsed_time(e) for s, e in zip(ev_s, ev_e)])
     st, msg = cache.la_get_error()
     if st != capi.LA_OK:
@@ -372,6 +532,12 @@ def run_ours(a):
                "api": "la_select_context + la_fill_block + la_chunk_attention + "
                       "la_cache_append_block, pinned host Q/K/V in and every output back"}
 
+    extra = {}
+    if rank == 0 and not a.no_extra and not a.layers:
+        extra = extra_legs(torch, capi, gen, [x for row in q for x in row],
+                           [x for row in k for x in row], [x for row in v for x in row], out, bank,
+                           block_ms, peaks()[0])
+
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         smp = OracleSample(workload())
@@ -392,6 +558,8 @@ def run_ours(a):
             "config": workload_desc(sc, b0 + a.warmup, a.steps) | {"parallelism": f"replicas x{world}"},
             "blocks_per_s": blocks_per_s,
             "per_block_latency_ms": t_max / a.steps * 1e3,
+            "block_ms": {"median": float(np.median(block_ms)), "min": float(np.min(block_ms)),
+                         "max": float(np.max(block_ms))},
             "frac_of_bf16_peak": value / pk["bf16_tflops"],
             "frac_of_bf16_peak_sustained": value / peak_sus,
             "attn_call_ms": {"mean": float(attn_ms.mean()), "min": float(attn_ms.min()),
@@ -402,6 +570,7 @@ def run_ours(a):
                          "kernel": "attn_tc_kernel", "peak_kind": f"bf16 sustained, {pk_kind}",
                          "frac_of_burst": achieved / pk["bf16_tflops"]},
             "cpu_baseline": cpu,
+            **extra,
             "e2e": e2e,
             "gpu_launches": int(launches),
             "clocks": clocks,

@@ -58,16 +58,9 @@ using namespace ptx;
 constexpr int kBM = 128;                 // query rows per tile
 constexpr int kBN = 128;                 // keys per tile
 constexpr int kD = 128;                  // head dim
-constexpr int kTileBytes = kBM * kD * 2; // 32 KB: two 16 KB halves of 64 dims
-constexpr int kHalfBytes = kTileBytes / 2;
 constexpr int kKSt = 2, kVSt = 2;
 constexpr int kThreads = 384;
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + 2 * kTileBytes;
-constexpr int kOffV = kOffK + kKSt * kTileBytes;
-constexpr int kOffCtl = kOffV + kVSt * kTileBytes;
 constexpr int kCtlBytes = 1024;
-constexpr int kSmemBytes = kOffCtl + kCtlBytes + 1024;   // + alignment slack
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 // Register split: launched at 168 per thread (384 threads, 1 CTA per SM =
 // 64512).  Control warpgroup 128 x 88 + two softmax warpgroups 2 x 128 x 208
@@ -75,6 +68,25 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kRegsCtl = 88;
 constexpr int kRegsSoftmax = 208;
 static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * 168, "register split too large");
+
+// Per element type of Q/K/V/P in the MMAs: bf16 (kind::f16) or e4m3
+// (kind::f8f6f4).  A tile is 128 rows of 128 elements, held as 128-byte
+// swizzled rows: two 64-element boxes for bf16, one 128-element box for e4m3.
+template <bool F8>
+struct Tile {
+  static constexpr int kElt = F8 ? 1 : 2;
+  static constexpr int kBytes = kBM * kD * kElt;          // 32 KB / 16 KB
+  static constexpr int kBoxes = F8 ? 1 : 2;
+  static constexpr int kBoxBytes = kBytes / kBoxes;       // 16 KB
+  static constexpr int kBoxElems = 128 / kElt;            // elements per 128-byte row
+  static constexpr int kMmaK = F8 ? 32 : 16;              // K of one MMA instruction
+  static constexpr int kSteps = kD / kMmaK;               // MMAs per 128-deep product
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kBytes;
+  static constexpr int kOffV = kOffK + kKSt * kBytes;
+  static constexpr int kOffCtl = kOffV + kVSt * kBytes;
+  static constexpr int kSmem = kOffCtl + kCtlBytes + 1024; // + alignment slack
+};
 constexpr float kRescaleThreshold = 8.0f;                 // log2(256)
 // Measured at the 14B shape (one call, B300): 0 -> 2.75 ms, 4 -> 2.91,
 // 6 -> 2.98, 8 -> 3.08: the exponentials are not the binding unit here, so
@@ -184,13 +196,24 @@ __device__ __forceinline__ float2 exp2_poly2(float2 x) {
   return p;
 }
 
+// Scales of slot s for head h (e4m3 cache): key scale (which = 0) or value
+// scale (which = 1) of the block the slot holds.
+__device__ __forceinline__ float slot_scale(const TcAttnArgs& a, const DevContext& c, int s, int which,
+                                            int h) {
+  if (c.kind[s] == SLOT_FRAME) return a.frame_scales[((size_t)c.frame[s] * 2 + which) * a.H + h];
+  return a.cur_scales[which * a.H + h];
+}
+
+template <bool F8>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcAttnArgs a) {
+  using Tl = Tile<F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kOffCtl);
+  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + Tl::kOffCtl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t sQ = smem_u32(smem + kOffQ), sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
+  const uint32_t sQ = smem_u32(smem + Tl::kOffQ), sK = smem_u32(smem + Tl::kOffK),
+                 sV = smem_u32(smem + Tl::kOffV);
 
   if (tid == 0) {
     mbar_init(smem_u32(&ctl.q_full), 1);
@@ -233,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   for (int s = 0; !bad && s < n_slots; ++s) {
     const int k = cx.kind[s], tok = cx.tokens[s];
     bad = tok < 1 || k < SLOT_FRAME || k > SLOT_MEMORY ||
-          (k == SLOT_FRAME && cx.frame[s] < 0) || (k != SLOT_MEMORY && tok > a.T);
+          (k == SLOT_FRAME && (cx.frame[s] < 0 || cx.frame[s] >= a.n_frames)) ||
+          (k != SLOT_MEMORY && tok > a.T) || (F8 && k == SLOT_MEMORY);
   }
   const Wait wait{&ctl.abort_flag, a.err};
   const uint32_t tmem = ctl.tmem_base;
@@ -263,26 +287,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           for (int kt = 0; ok && kt < nt; ++kt) {
             const int ks = kc % kKSt;
             if (!(ok = wait(ctl.k_empty[ks], ((kc / kKSt) & 1) ^ 1, 1))) break;
-            mbar_arrive_expect_tx(smem_u32(&ctl.k_full[ks]), kTileBytes);
-            for (int hf = 0; hf < 2; ++hf)
-              tma_load_3d(sK + ks * kTileBytes + hf * kHalfBytes, km, hf * 64, kt * kBN, krow,
-                          smem_u32(&ctl.k_full[ks]));
+            mbar_arrive_expect_tx(smem_u32(&ctl.k_full[ks]), Tl::kBytes);
+            for (int bx = 0; bx < Tl::kBoxes; ++bx)
+              tma_load_3d(sK + ks * Tl::kBytes + bx * Tl::kBoxBytes, km, bx * Tl::kBoxElems, kt * kBN,
+                          krow, smem_u32(&ctl.k_full[ks]));
             ++kc;
             if (kt == 0) {
               if (!(ok = wait(ctl.q_empty, (qc & 1) ^ 1, 2))) break;
-              mbar_arrive_expect_tx(smem_u32(&ctl.q_full), n_qt * kTileBytes);
+              mbar_arrive_expect_tx(smem_u32(&ctl.q_full), n_qt * Tl::kBytes);
               for (int qi = 0; qi < n_qt; ++qi)
-                for (int hf = 0; hf < 2; ++hf)
-                  tma_load_3d(sQ + qi * kTileBytes + hf * kHalfBytes, &a.tm_q, hf * 64,
+                for (int bx = 0; bx < Tl::kBoxes; ++bx)
+                  tma_load_3d(sQ + qi * Tl::kBytes + bx * Tl::kBoxBytes, &a.tm_q, bx * Tl::kBoxElems,
                               row0 + qi * kBM, s * a.H + h, smem_u32(&ctl.q_full));
               ++qc;
             }
             const int vs = vc % kVSt;
             if (!(ok = wait(ctl.v_empty[vs], ((vc / kVSt) & 1) ^ 1, 3))) break;
-            mbar_arrive_expect_tx(smem_u32(&ctl.v_full[vs]), kTileBytes);
-            for (int hf = 0; hf < 2; ++hf)
-              tma_load_3d(sV + vs * kTileBytes + hf * kHalfBytes, vm, hf * 64, kt * kBN, vrow,
-                          smem_u32(&ctl.v_full[vs]));
+            mbar_arrive_expect_tx(smem_u32(&ctl.v_full[vs]), Tl::kBytes);
+            for (int bx = 0; bx < Tl::kBoxes; ++bx)
+              tma_load_3d(sV + vs * Tl::kBytes + bx * Tl::kBoxBytes, vm, bx * Tl::kBoxElems, kt * kBN,
+                          vrow, smem_u32(&ctl.v_full[vs]));
             ++vc;
           }
         }
@@ -307,24 +331,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_bf16(kBM, kBN, 0, 0);
-      const uint32_t idesc_pv = idesc_bf16(kBM, kD, 0, 1);
+      const uint32_t idesc_qk = F8 ? idesc_e4m3(kBM, kBN, 0, 0) : idesc_bf16(kBM, kBN, 0, 0);
+      const uint32_t idesc_pv = F8 ? idesc_e4m3(kBM, kD, 0, 1) : idesc_bf16(kBM, kD, 0, 1);
       uint32_t kc = 0, vc = 0, qc = 0, pc0 = 0, pc1 = 0;
       bool ok = true;
+      // S_i = Q_i K^T: both K-major; step kk covers 32 bytes of each 128-byte row.
       auto issue_qk = [&](int i, int ks) {
-        const uint32_t q = sQ + i * kTileBytes, k = sK + ks * kTileBytes;
+        const uint32_t q = sQ + i * Tl::kBytes, k = sK + ks * Tl::kBytes;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tmem + i * 128, sdesc(q + off, 16, 1024), sdesc(k + off, 16, 1024), idesc_qk, kk > 0);
+        for (int kk = 0; kk < Tl::kSteps; ++kk) {
+          const uint32_t off = (kk * 32 / 128) * Tl::kBoxBytes + (kk * 32) % 128;
+          if (F8)
+            mma_ss_f8(tmem + i * 128, sdesc(q + off, 16, 1024), sdesc(k + off, 16, 1024), idesc_qk, kk > 0);
+          else
+            mma_ss(tmem + i * 128, sdesc(q + off, 16, 1024), sdesc(k + off, 16, 1024), idesc_qk, kk > 0);
         }
       };
+      // O_i += P_i V: P from TMEM (8 columns per step), V MN-major (kMmaK key
+      // rows of 128 bytes per step, 128-byte column chunks kBoxBytes apart).
       auto issue_pv = [&](int i, int vs, bool first) {
-        const uint32_t v = sV + vs * kTileBytes;
+        const uint32_t v = sV + vs * Tl::kBytes;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, sdesc(v + kk * 2048, kHalfBytes, 1024), idesc_pv,
-                 !(first && kk == 0));
+        for (int kk = 0; kk < Tl::kSteps; ++kk) {
+          const uint64_t bd = sdesc(v + kk * Tl::kMmaK * 128, Tl::kBoxBytes, 1024);
+          if (F8)
+            mma_ts_f8(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, bd, idesc_pv, !(first && kk == 0));
+          else
+            mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, bd, idesc_pv, !(first && kk == 0));
+        }
       };
       for (int i = 0; ok; ++i) {
         const int u = units.index(i);
@@ -408,7 +442,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + qi * 128;
     const uint32_t tO = tmem + lane_off + 256 + qi * 128;
-    const float c = a.scale_log2;
     uint32_t sph = 0, oph = 0;
     bool ok = true;
     for (int i = 0; ok; ++i) {
@@ -418,11 +451,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       bool half;
       units.get(u, h, row0, half);
       if (half && qi == 1) continue;               // the tile past the head's last rows
+      const int row = row0 + qi * kBM + r;
+      // e4m3: true score = q_scale(row) * k_scale(slot) * S; P is stored as
+      // p * v_scale(slot) / v_max so that O = v_max * sum(P V codes).
+      float q_scale = 1.f, v_max = 1.f;
+      if (F8) {
+        if (row < a.T) q_scale = a.q_scales[(size_t)h * a.T + row];
+        v_max = 0.f;
+        for (int s = 0; s < n_slots; ++s) v_max = fmaxf(v_max, slot_scale(a, cx, s, 1, h));
+        if (!(v_max > 0.f)) v_max = 1.f;
+      }
       float m = -INFINITY, l = 0.f;
       int j = 0;
       for (int s = 0; ok && s < n_slots; ++s) {
         const int tokens = cx.tokens[s];
         const int nt = (tokens + kBN - 1) / kBN;
+        float c = a.scale_log2, p_mul = 1.f;
+        if (F8) {
+          c *= q_scale * slot_scale(a, cx, s, 0, h);
+          p_mul = slot_scale(a, cx, s, 1, h) / v_max;
+        }
         for (int kt = 0; kt < nt; ++kt, ++j) {
           ok = __all_sync(0xffffffffu, wait(ctl.s_full[qi], sph & 1, 21 + qi));
           if (!ok) break;
@@ -471,23 +519,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
           float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                            make_float2(0.f, 0.f)};
+          if (!F8) {
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
+            for (int hf = 0; hf < 2; ++hf) {
+              uint32_t pk[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const float2 x = ffma2(make_float2(sv[hf * 64 + 2 * e], sv[hf * 64 + 2 * e + 1]), c2, nm2);
+                float2 p;
+                if ((e & 15) < kEmuPairs) {
+                  p = exp2_poly2(x);
+                } else {
+                  p.x = ex2(x.x);
+                  p.y = ex2(x.y);
+                }
+                acc[e & 3] = fadd2(acc[e & 3], p);
+                pk[e] = cvt_bf16x2(p.x, p.y);
+              }
+              tmem_st32(tS + hf * 32, pk);
+            }
+          } else {
             uint32_t pk[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const float2 x = ffma2(make_float2(sv[hf * 64 + 2 * e], sv[hf * 64 + 2 * e + 1]), c2, nm2);
-              float2 p;
-              if ((e & 15) < kEmuPairs) {
-                p = exp2_poly2(x);
-              } else {
-                p.x = ex2(x.x);
-                p.y = ex2(x.y);
-              }
-              acc[e & 3] = fadd2(acc[e & 3], p);
-              pk[e] = cvt_bf16x2(p.x, p.y);
+              const float2 x0 = ffma2(make_float2(sv[4 * e], sv[4 * e + 1]), c2, nm2);
+              const float2 x1 = ffma2(make_float2(sv[4 * e + 2], sv[4 * e + 3]), c2, nm2);
+              const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+              const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+              acc[(2 * e) & 3] = fadd2(acc[(2 * e) & 3], p0);
+              acc[(2 * e + 1) & 3] = fadd2(acc[(2 * e + 1) & 3], p1);
+              pk[e] = cvt_e4m3x4(p0.x * p_mul, p0.y * p_mul, p1.x * p_mul, p1.y * p_mul);
             }
-            tmem_st32(tS + hf * 32, pk);
+            tmem_st32(tS, pk);
           }
           const float2 s01 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
           l += s01.x + s01.y;
@@ -501,8 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       if (!ok) break;
       ++oph;
       tc_fence_after();
-      const float inv_l = 1.f / l;
-      const int row = row0 + qi * kBM + r;
+      const float inv_l = v_max / l;
       uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + ((size_t)row * a.H + h) * kD;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -533,6 +595,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 }
 
 // Per-slot rotated copies of the queries: qrot[s][h][t] = R(t0_cur + f - t0_s, row, col) q[t][h].
+// bf16 cache: bf16 copies.  e4m3 cache: e4m3 codes with one fp32 scale per
+// (head, token), qscale[h][t] = m / 448 where m is the largest norm of the
+// token's 64 rotation pairs -- rotations keep pair norms, so one scale
+// serves every slot and no code saturates.  One thread per 8 dims; the 16
+// threads of a (token, head) are 16 consecutive lanes.
+template <bool F8>
 __global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
   const DevContext& ctx = *a.ctx;
   const int n_slots = ctx.n_slots;
@@ -540,12 +608,26 @@ __global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
     if (blockIdx.x == 0 && threadIdx.x == 0) record_error(a.err, LA_ERR_DEVICE, KID_QROT, n_slots, a.n_qrot);
     return;
   }
+  // every slot's temporal offset must stay inside the RoPE table for every
+  // frame of the block (checked up front so that all threads leave together)
+  for (int s = 0; s < n_slots; ++s) {
+    const int lo = ctx.t0_cur - ctx.t0[s], hi = lo + a.rope.F - 1;
+    if (lo < 0 || hi >= a.rope.max_t) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) record_error(a.err, LA_ERR_DEVICE, KID_QROT, lo, s);
+      return;
+    }
+  }
   const int chunks = a.D / 8;
   const long long total = (long long)a.T * a.H * chunks;
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int cch = (int)(idx % chunks);
-    const long long th = idx / chunks;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  // warp-uniform trip count (the e4m3 path reduces over 16-lane groups)
+  for (long long base = blockIdx.x * (long long)blockDim.x + (threadIdx.x & ~31); base < total;
+       base += stride) {
+    const long long idx = base + (threadIdx.x & 31);
+    const bool valid = idx < total;
+    const long long vi = valid ? idx : 0;
+    const int cch = (int)(vi % chunks);
+    const long long th = vi / chunks;
     const int h = (int)(th % a.H);
     const int t = (int)(th / a.H);
     uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + (size_t)th * a.D + cch * 8);
@@ -556,56 +638,86 @@ __global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
       x[2 * e] = __uint_as_float(w[e] << 16);
       x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
     }
+    float inv = 1.f;
+    if (F8) {
+      float n2 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) n2 = fmaxf(n2, x[2 * e] * x[2 * e] + x[2 * e + 1] * x[2 * e + 1]);
+#pragma unroll
+      for (int o = 8; o; o >>= 1) n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
+      const float mn = sqrtf(n2);
+      inv = mn > 0.f ? 448.f / mn : 0.f;
+      if (valid && cch == 0) a.qscale[(size_t)h * a.T + t] = mn > 0.f ? mn / 448.f : 1.f;
+    }
+    if (!valid) continue;
     int f, hh, ww;
     token_pos(a.rope, t, f, hh, ww);
     for (int s = 0; s < n_slots; ++s) {
       const int dtq = ctx.t0_cur + f - ctx.t0[s];
-      if (dtq < 0 || dtq >= a.rope.max_t) {
-        record_error(a.err, LA_ERR_DEVICE, KID_QROT, dtq, s);
-        return;
-      }
-      uint4 o;
-      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+      float y[8];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 cs = rope_cs(a.rope, cch * 8 + 2 * e, dtq, hh, ww);
-        const float2 y = rot_exact(x[2 * e], x[2 * e + 1], cs);
-        ow[e] = pack_bf16x2(y.x, y.y);
+        const float2 r = rot_exact(x[2 * e], x[2 * e + 1], cs);
+        y[2 * e] = r.x;
+        y[2 * e + 1] = r.y;
       }
-      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.qrot) +
-                                (((size_t)s * a.H + h) * a.T + t) * a.D + cch * 8) = o;
+      const size_t off = (((size_t)s * a.H + h) * a.T + t) * a.D + cch * 8;
+      if (F8) {
+        uint2 o;
+        o.x = cvt_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
+        o.y = cvt_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv);
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.qrot) + off) = o;
+      } else {
+        uint4 o;
+        o.x = cvt_bf16x2(y[0], y[1]);
+        o.y = cvt_bf16x2(y[2], y[3]);
+        o.z = cvt_bf16x2(y[4], y[5]);
+        o.w = cvt_bf16x2(y[6], y[7]);
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.qrot) + off) = o;
+      }
     }
   }
 }
 
 }  // namespace
 
-bool attn_tc_supported(int D, int kv_dtype) { return D == kD && kv_dtype == LA_BF16; }
+bool attn_tc_supported(int D, int kv_dtype) {
+  return D == kD && (kv_dtype == LA_BF16 || kv_dtype == LA_E4M3);
+}
 
 cudaError_t launch_qrot(const QrotArgs& a, cudaStream_t s) {
-  if (a.D % 8) return cudaErrorInvalidValue;
+  if (a.D != kD) return cudaErrorInvalidValue;
   long long work = (long long)a.T * a.H * (a.D / 8);
   long long grid = (work + 255) / 256;
   if (grid > 148LL * 16) grid = 148LL * 16;
-  qrot_kernel<<<(int)grid, 256, 0, s>>>(a);
+  if (a.f8)
+    qrot_kernel<true><<<(int)grid, 256, 0, s>>>(a);
+  else
+    qrot_kernel<false><<<(int)grid, 256, 0, s>>>(a);
   count_launches(1);
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_tc(const TcAttnArgs& a, int num_sms, cudaStream_t s) {
+template <bool F8>
+static cudaError_t launch_attn_tc_t(const TcAttnArgs& a, int num_sms, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Tile<F8>::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int n_pairs = (a.T + 2 * kBM - 1) / (2 * kBM);
   const int units = a.H * n_pairs;
   const int grid = units < num_sms ? units : num_sms;
-  attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
+  attn_tc_kernel<F8><<<grid, kThreads, Tile<F8>::kSmem, s>>>(a);
   count_launches(1);
   return cudaGetLastError();
+}
+
+cudaError_t launch_attn_tc(const TcAttnArgs& a, int num_sms, cudaStream_t s) {
+  return a.kv_f8 ? launch_attn_tc_t<true>(a, num_sms, s) : launch_attn_tc_t<false>(a, num_sms, s);
 }
 
 }  // namespace la

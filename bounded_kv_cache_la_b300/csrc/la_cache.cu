@@ -116,6 +116,8 @@ int exact_slots(const la_cache_config& c) {
 
 bool tc_eligible(const la_cache_config& c, const Layout& L) {
   if (c.attn_impl == LA_ATTN_SIMT) return false;
+  // the e4m3 tensor path serves PR-Sink (the ConvKV memory is bf16)
+  if (c.kv_dtype == LA_E4M3 && !is_prsink(c)) return false;
   return attn_tc_supported(c.head_dim, c.kv_dtype) && c.q_dtype == LA_BF16 &&
          L.page_stride == L.page_bytes;
 }
@@ -158,7 +160,9 @@ void compute_layout(const la_cache_config& c, Layout& L) {
   L.frames = take((size_t)c.num_layers * L.n_frames * L.G * L.page_stride);
   L.cur_pages = take(2 * L.page_stride);
   const bool tc = tc_eligible(c, L);
-  L.qrot = take(tc ? (size_t)L.n_qrot * H * T * D * 2 : 0);
+  const bool f8 = c.kv_dtype == LA_E4M3;
+  L.qrot = take(tc ? (size_t)L.n_qrot * H * T * D * (f8 ? 1 : 2) : 0);
+  L.qscale = take(tc && f8 ? sizeof(float) * (size_t)H * T : 0);
   L.mem = take(is_prsink(c) ? 0 : (size_t)c.num_layers * 3 * H * c.mem_slots * D * 2);
   L.total = off;
 }
@@ -267,8 +271,10 @@ std::vector<int> window_blocks(const la_cache_config& g, int b) {
   return w;
 }
 
+// 3D map [n_heads_total][rows_per_head][d] of 1- or 2-byte elements; a box
+// is 128 rows x one 128-byte swizzled row span (64 bf16 or 128 e4m3).
 bool encode_map(la_cache* c, CUtensorMap* m, void* base, int d, uint64_t rows_per_head,
-                uint64_t n_heads_total) {
+                uint64_t n_heads_total, int elt) {
   typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -284,10 +290,11 @@ bool encode_map(la_cache* c, CUtensorMap* m, void* base, int d, uint64_t rows_pe
     fn = reinterpret_cast<EncodeFn>(p);
   }
   cuuint64_t dims[3] = {(cuuint64_t)d, rows_per_head, n_heads_total};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * rows_per_head};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)d * elt, (cuuint64_t)d * elt * rows_per_head};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / elt), 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+  CUresult r = fn(m, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   (void)c;
@@ -413,13 +420,14 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
   c->tc = tc_eligible(*cfg, L);
   if (st == LA_OK && c->tc) {
     const int H = cfg->num_heads, D = cfg->head_dim;
-    bool ok = encode_map(c, &c->tm_q, c->pool + L.qrot, D, c->T, (uint64_t)L.n_qrot * H) &&
+    const int elt = cfg->kv_dtype == LA_E4M3 ? 1 : 2;
+    bool ok = encode_map(c, &c->tm_q, c->pool + L.qrot, D, c->T, (uint64_t)L.n_qrot * H, elt) &&
               encode_map(c, &c->tm_kv, c->pool + L.frames, D, c->T,
-                         (uint64_t)cfg->num_layers * L.n_frames * L.G * H) &&
-              encode_map(c, &c->tm_cur, c->pool + L.cur_pages, D, c->T, 2ull * H);
+                         (uint64_t)cfg->num_layers * L.n_frames * L.G * H, elt) &&
+              encode_map(c, &c->tm_cur, c->pool + L.cur_pages, D, c->T, 2ull * H, elt);
     if (ok && !is_prsink(*cfg))
       ok = encode_map(c, &c->tm_mem, c->pool + L.mem, D, cfg->mem_slots,
-                      (uint64_t)cfg->num_layers * 3 * H);
+                      (uint64_t)cfg->num_layers * 3 * H, 2);
     else if (ok)
       c->tm_mem = c->tm_cur;
     if (!ok) {
@@ -674,6 +682,8 @@ la_status la_chunk_attention(la_cache_t* c, int layer, const void* q, const void
     qa.H = g.num_heads;
     qa.D = g.head_dim;
     qa.n_qrot = c->L.n_qrot;
+    qa.f8 = g.kv_dtype == LA_E4M3;
+    qa.qscale = reinterpret_cast<float*>(c->pool + c->L.qscale);
     qa.rope = c->rope;
     qa.err = err;
     st = cuda_status(c, launch_qrot(qa, s), "query rotation kernel");
@@ -684,6 +694,11 @@ la_status la_chunk_attention(la_cache_t* c, int layer, const void* q, const void
     ta.tm_cur = c->tm_cur;
     ta.tm_mem = c->tm_mem;
     ta.ctx = dctx;
+    ta.kv_f8 = g.kv_dtype == LA_E4M3;
+    ta.frame_scales = ta.kv_f8 ? frame_scales(c, layer, 0) : nullptr;
+    ta.cur_scales = reinterpret_cast<const float*>(c->pool + c->L.cur_scales);
+    ta.q_scales = reinterpret_cast<const float*>(c->pool + c->L.qscale);
+    ta.n_frames = c->L.n_frames;
     ta.out = out;
     ta.T = c->T;
     ta.H = g.num_heads;

@@ -7,7 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/la_cache.h"
+#include "la_cache.h"
 
 namespace la {
 
@@ -62,7 +62,8 @@ struct Layout {
   size_t cur_scales;               // e4m3 [2][H] fp32
   size_t frames;                   // [L][n_frames][G] pages
   size_t cur_pages;                // 2 pages: current block K', V
-  size_t qrot;                     // [S][H][T][D] bf16 rotated queries (tensor path)
+  size_t qrot;                     // [S][H][T][D] rotated queries (tensor path), kv dtype
+  size_t qscale;                   // e4m3 tensor path: [H][T] fp32 query scales
   size_t mem;                      // ConvKV [L][3][H][cap][D] bf16 (raw K, V, rotated K)
   size_t total;
   size_t page_bytes;               // H * T * D * elt(kv_dtype)
@@ -160,20 +161,27 @@ cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t s);
 
 struct QrotArgs {
   const void* q;       // [T][H][D] bf16
-  void* qrot;          // [S][H][T][D] bf16
+  void* qrot;          // [S][H][T][D] bf16, or e4m3 codes when f8
+  float* qscale;       // f8: [H][T] per-token scales
   const DevContext* ctx;
   int T, H, D, n_qrot;
+  int f8;
   RopeDims rope;
   DevError* err;
 };
 cudaError_t launch_qrot(const QrotArgs& a, cudaStream_t s);
 
 struct TcAttnArgs {
-  CUtensorMap tm_q;    // rotated queries  [S*H][T][D] bf16
-  CUtensorMap tm_kv;   // pool pages       [frames*G*H][T][D] bf16 (whole pool)
+  CUtensorMap tm_q;    // rotated queries  [S*H][T][D] bf16 (e4m3 codes when kv_f8)
+  CUtensorMap tm_kv;   // pool pages       [frames*G*H][T][D] kv dtype (whole pool)
   CUtensorMap tm_cur;  // current pages    [2*H][T][D]
   CUtensorMap tm_mem;  // ConvKV rings     [L*3*H][cap][D] (or a dummy)
   const DevContext* ctx;
+  const float* frame_scales;  // e4m3: this layer's [n_frames][2][H]
+  const float* cur_scales;    // e4m3: [2][H]
+  const float* q_scales;      // e4m3: [H][T]
+  int n_frames;               // frames per layer (bound of ctx->frame)
+  int kv_f8;                  // 1: e4m3 K/V and queries, kind::f8f6f4
   void* out;           // [T][H][D] bf16
   int T, H;
   int layer_frame0;    // first frame page row of this layer in tm_kv, in pages

@@ -16,6 +16,12 @@ TOL = {
     "f32": dict(max_abs=2e-5, mean_abs=2e-6, rel=1e-4),
     "bf16": dict(max_abs=2e-2, mean_abs=2e-3, rel=1.5e-2),
     "e4m3": dict(max_abs=8e-2, mean_abs=8e-3, rel=3e-2),
+    # e4m3 K/V on the tensor cores: Q and P are e4m3 too (the products run
+    # in kind::f8f6f4).  Each adds RNE rounding of up to 2^-4 relative per
+    # element; at the FP8 stress shape (42120 keys) that gives ~3.7% relative
+    # L2 error against the oracle's exact-Q, exact-P output (simulated in
+    # NumPy), while the absolute errors stay ~40x inside the stated bounds.
+    "e4m3_tc": dict(max_abs=8e-2, mean_abs=8e-3, rel=6e-2),
 }
 
 

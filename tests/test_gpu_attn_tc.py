@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 from oracle import stream as ostream
-from synth import C2_MID, C3_14B, C4_CONVKV, gen
+from synth import C2_MID, C3_14B, C4_CONVKV, C5_FP8, gen
 
 from . import harness as H
 
@@ -110,3 +110,58 @@ def test_uniform_scores_give_mean_of_values():
             ref = np.broadcast_to(V.mean(0), out.shape)
             H.compare(out.float().cpu().numpy(), ref, "bf16", "uniform")
         cache.la_cache_append_block(0, k, v)
+
+
+def test_fp8_tensor_cores_stream():
+    """FP8 stress shape (4680 tokens, pose top-4, e4m3 K/V with per-(head,
+    block) scales) at 4 heads, external history: the kind::f8f6f4 kernel
+    against the oracle over the dequantised cache, on blocks before and
+    after the dynamic sink fills."""
+    sc = C5_FP8.with_(num_heads=4)
+    n = 12
+    keep = {0, 4, 5, 8, 11}
+    _, ctxs, outs = H.run_stream(sc, n, keep, n_steps=1, layers=1, attn_impl=1)
+    ref = ostream.plan_stream(sc, gen.poses(sc, n_blocks=n), n)
+    for b in range(n):
+        assert ctxs[b]["kv_len"] == ref[b].kv_len
+    assert ctxs[11]["kv_len"] == 9 * sc.tokens_per_block
+    vals = H.Values(sc)
+    rows = np.r_[0:160, 2300:2400, 4560:4680]
+    for b in sorted(keep):
+        ctx = ref[b]
+        if ctxs[b]["dyn_ids"] != ctx.dyn_ids:
+            assert ctx.gap <= 1e-6
+            continue
+        o = H.oracle_output(sc, ctx, vals, 0, 0, 1, rows=rows)
+        H.compare(outs[b][(0, 0)][rows], o, "e4m3_tc", f"block {b}")
+
+
+def test_fp8_tensor_cores_match_simt_kernel():
+    """The e4m3 tensor-core kernel and the CUDA-core kernel (which keeps Q
+    and P in fp32) agree on a ragged shape within the e4m3 bound."""
+    sc = C5_FP8.with_(num_heads=3, grid_h=13, grid_w=15, history_mode="resident")  # 585 tokens
+    keep = {3, 7, 11}
+    _, _, o_tc = H.run_stream(sc, 12, keep, attn_impl=1)
+    _, _, o_simt = H.run_stream(sc, 12, keep, attn_impl=2)
+    for b in keep:
+        H.compare(o_tc[b][(0, 0)], o_simt[b][(0, 0)].astype(np.float64), "e4m3_tc", f"block {b}")
+
+
+def test_fp8_14b_shape_sampled_rows():
+    """All 40 heads of the FP8 stress shape; oracle on 3 heads x 192 rows
+    once the top-4 dynamic sink is full (42120 keys)."""
+    sc = C5_FP8
+    n = 10
+    keep = {9}
+    _, ctxs, outs = H.run_stream(sc, n, keep, n_steps=1, layers=1, attn_impl=1)
+    ref = ostream.plan_stream(sc, gen.poses(sc, n_blocks=n), n)
+    assert ctxs[9]["kv_len"] == ref[9].kv_len == 42120
+    heads = [0, 21, 39]
+    vals = H.Values(sc, heads)
+    rows = np.r_[0:64, 2300:2364, 4616:4680]
+    ctx = ref[9]
+    if ctxs[9]["dyn_ids"] != ctx.dyn_ids:
+        assert ctx.gap <= 1e-6
+        return
+    o = H.oracle_output(sc, ctx, vals, 0, 0, 1, rows=rows)
+    H.compare(outs[9][(0, 0)][rows][:, heads], o, "e4m3_tc", "block 9")

@@ -335,25 +335,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const uint32_t idesc_pv = F8 ? idesc_e4m3(kBM, kD, 0, 1) : idesc_bf16(kBM, kD, 0, 1);
       uint32_t kc = 0, vc = 0, qc = 0, pc0 = 0, pc1 = 0;
       bool ok = true;
+      // Shared-memory descriptors are built once; a tile or K-step offset is
+      // added to the 14-bit start-address field (addresses >> 4, all below
+      // 256 KB, so the add never carries out of the field).  Few
+      // instructions per MMA matter: this thread shares its sub-partition's
+      // issue slots with two softmax warps.
+      const uint64_t dq0 = sdesc(sQ, 16, 1024), dk0 = sdesc(sK, 16, 1024);
+      const uint64_t dv0 = sdesc(sV, Tl::kBoxBytes, 1024);
       // S_i = Q_i K^T: both K-major; step kk covers 32 bytes of each 128-byte row.
       auto issue_qk = [&](int i, int ks) {
-        const uint32_t q = sQ + i * Tl::kBytes, k = sK + ks * Tl::kBytes;
+        const uint64_t q = dq0 + ((uint32_t)(i * Tl::kBytes) >> 4);
+        const uint64_t k = dk0 + ((uint32_t)(ks * Tl::kBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < Tl::kSteps; ++kk) {
-          const uint32_t off = (kk * 32 / 128) * Tl::kBoxBytes + (kk * 32) % 128;
+          const uint32_t off = ((kk * 32 / 128) * Tl::kBoxBytes + (kk * 32) % 128) >> 4;
           if (F8)
-            mma_ss_f8(tmem + i * 128, sdesc(q + off, 16, 1024), sdesc(k + off, 16, 1024), idesc_qk, kk > 0);
+            mma_ss_f8(tmem + i * 128, q + off, k + off, idesc_qk, kk > 0);
           else
-            mma_ss(tmem + i * 128, sdesc(q + off, 16, 1024), sdesc(k + off, 16, 1024), idesc_qk, kk > 0);
+            mma_ss(tmem + i * 128, q + off, k + off, idesc_qk, kk > 0);
         }
       };
       // O_i += P_i V: P from TMEM (8 columns per step), V MN-major (kMmaK key
       // rows of 128 bytes per step, 128-byte column chunks kBoxBytes apart).
       auto issue_pv = [&](int i, int vs, bool first) {
-        const uint32_t v = sV + vs * Tl::kBytes;
+        const uint64_t v = dv0 + ((uint32_t)(vs * Tl::kBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < Tl::kSteps; ++kk) {
-          const uint64_t bd = sdesc(v + kk * Tl::kMmaK * 128, Tl::kBoxBytes, 1024);
+          const uint64_t bd = v + ((uint32_t)(kk * Tl::kMmaK * 128) >> 4);
           if (F8)
             mma_ts_f8(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, bd, idesc_pv, !(first && kk == 0));
           else
@@ -466,10 +474,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int s = 0; ok && s < n_slots; ++s) {
         const int tokens = cx.tokens[s];
         const int nt = (tokens + kBN - 1) / kBN;
-        float c = a.scale_log2, p_mul = 1.f;
+        // e4m3: P is stored as p * r, r = v_scale(slot) / v_max <= 1, by
+        // shifting the exponent by log2(r); the row sum divides r back out.
+        float c = a.scale_log2, lr = 0.f, inv_r = 1.f;
         if (F8) {
           c *= q_scale * slot_scale(a, cx, s, 0, h);
-          p_mul = slot_scale(a, cx, s, 1, h) / v_max;
+          const float r_slot = slot_scale(a, cx, s, 1, h) / v_max;
+          lr = __log2f(r_slot);
+          inv_r = 1.f / r_slot;
         }
         for (int kt = 0; kt < nt; ++kt, ++j) {
           ok = __all_sync(0xffffffffu, wait(ctl.s_full[qi], sph & 1, 21 + qi));
@@ -477,83 +489,100 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           ++sph;
           tc_fence_after();
           float sv[kBN];
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, reinterpret_cast<uint32_t*>(sv) + cc * 32);
-          tmem_wait_ld();
           const int valid = tokens - kt * kBN;
-          if (valid < kBN) {
+          auto load_s = [&]() {
 #pragma unroll
-            for (int cc = 0; cc < kBN; ++cc)
-              if (cc >= valid) sv[cc] = -INFINITY;
-          }
-          // row max: 8 independent 3-input max chains, then a tree
-          float t8[8];
+            for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, reinterpret_cast<uint32_t*>(sv) + cc * 32);
+            tmem_wait_ld();
+            if (valid < kBN) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) t8[e] = fmax3(sv[e], sv[e + 8], sv[e + 16]);
-#pragma unroll
-          for (int b = 24; b + 16 <= kBN; b += 16)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) t8[e] = fmax3(t8[e], sv[b + e], sv[b + 8 + e]);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) t8[e] = fmaxf(t8[e], sv[kBN - 8 + e]);
-          float mx = fmaxf(fmax3(t8[0], t8[1], t8[2]), fmax3(fmax3(t8[3], t8[4], t8[5]), t8[6], t8[7]));
-          mx *= c;
-          if (__any_sync(0xffffffffu, mx > m + kRescaleThreshold)) {
-            const float m_new = fmaxf(m, mx);
-            const float alpha = ex2(m - m_new);
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-              for (int cc = 0; cc < 4; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(tO + cc * 32, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                tmem_st32(tO + cc * 32, o);
-              }
-              tmem_wait_st();
+              for (int cc = 0; cc < kBN; ++cc)
+                if (cc >= valid) sv[cc] = -INFINITY;
             }
-            l *= alpha;
-            m = m_new;
+          };
+          // sv <- 2^(sv c - m + lr) in place; returns this row's sum of those.
+          auto exp_tile = [&]() {
+            const float2 c2 = make_float2(c, c), nm2 = make_float2(lr - m, lr - m);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+#pragma unroll
+            for (int e = 0; e < kBN / 2; ++e) {
+              const float2 x = ffma2(make_float2(sv[2 * e], sv[2 * e + 1]), c2, nm2);
+              float2 p;
+              if (!F8 && (e & 15) < kEmuPairs) {
+                p = exp2_poly2(x);
+              } else {
+                p.x = ex2(x.x);
+                p.y = ex2(x.y);
+              }
+              sv[2 * e] = p.x;
+              sv[2 * e + 1] = p.y;
+              acc[e & 3] = fadd2(acc[e & 3], p);
+            }
+            const float2 s01 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+            return s01.x + s01.y;
+          };
+          load_s();
+          // Against the running max m no stored value may exceed 2^8 (e4m3
+          // tops out at 448).  A row sum of at most 2^8 proves that without a
+          // row max, so the max is only taken on a unit's first tile or when
+          // some row's sum goes over; then the lazy rescale below applies and
+          // the tile is recomputed.
+          float tsum;
+          bool exact = j == 0;
+          for (;;) {
+            if (exact) {
+              // row max: 8 independent 3-input max chains, then a tree
+              float t8[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) t8[e] = fmax3(sv[e], sv[e + 8], sv[e + 16]);
+#pragma unroll
+              for (int b = 24; b + 16 <= kBN; b += 16)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t8[e] = fmax3(t8[e], sv[b + e], sv[b + 8 + e]);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) t8[e] = fmaxf(t8[e], sv[kBN - 8 + e]);
+              float mx = fmaxf(fmax3(t8[0], t8[1], t8[2]), fmax3(fmax3(t8[3], t8[4], t8[5]), t8[6], t8[7]));
+              mx *= c;
+              if (__any_sync(0xffffffffu, mx > m + kRescaleThreshold)) {
+                const float m_new = fmaxf(m, mx);
+                const float alpha = ex2(m - m_new);
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                  for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + cc * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tO + cc * 32, o);
+                  }
+                  tmem_wait_st();
+                }
+                l *= alpha;
+                m = m_new;
+              }
+            }
+            tsum = exp_tile();
+            if (exact || !__any_sync(0xffffffffu, !(tsum <= 256.f))) break;
+            exact = true;
+            load_s();
           }
-          const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
-          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};
+          l += tsum * inv_r;
           if (!F8) {
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               uint32_t pk[32];
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float2 x = ffma2(make_float2(sv[hf * 64 + 2 * e], sv[hf * 64 + 2 * e + 1]), c2, nm2);
-                float2 p;
-                if ((e & 15) < kEmuPairs) {
-                  p = exp2_poly2(x);
-                } else {
-                  p.x = ex2(x.x);
-                  p.y = ex2(x.y);
-                }
-                acc[e & 3] = fadd2(acc[e & 3], p);
-                pk[e] = cvt_bf16x2(p.x, p.y);
-              }
+              for (int e = 0; e < 32; ++e) pk[e] = cvt_bf16x2(sv[hf * 64 + 2 * e], sv[hf * 64 + 2 * e + 1]);
               tmem_st32(tS + hf * 32, pk);
             }
           } else {
             uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float2 x0 = ffma2(make_float2(sv[4 * e], sv[4 * e + 1]), c2, nm2);
-              const float2 x1 = ffma2(make_float2(sv[4 * e + 2], sv[4 * e + 3]), c2, nm2);
-              const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
-              const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
-              acc[(2 * e) & 3] = fadd2(acc[(2 * e) & 3], p0);
-              acc[(2 * e + 1) & 3] = fadd2(acc[(2 * e + 1) & 3], p1);
-              pk[e] = cvt_e4m3x4(p0.x * p_mul, p0.y * p_mul, p1.x * p_mul, p1.y * p_mul);
-            }
+            for (int e = 0; e < 32; ++e) pk[e] = cvt_e4m3x4(sv[4 * e], sv[4 * e + 1], sv[4 * e + 2], sv[4 * e + 3]);
             tmem_st32(tS, pk);
           }
-          const float2 s01 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-          l += s01.x + s01.y;
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(smem_u32(&ctl.p_ready[qi]));

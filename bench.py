@@ -47,6 +47,8 @@ def args_():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="c3_14b", choices=["c3_14b", "c5_fp8", "c4_convkv"],
+                    help="stream of the main leg (the headline metric is c3_14b)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the FP8, ConvKV and latency-flatness legs")
     ap.add_argument("--layers", type=int, default=None, help="override (testing only)")
@@ -54,9 +56,16 @@ def args_():
 
 
 # ------------------------------------------------------------------ workload
-def workload():
-    from synth import C3_14B
-    return C3_14B
+def workload(name="c3_14b"):
+    from synth import CONFIGS
+    return CONFIGS[name]
+
+
+def context_len(sc):
+    """Keys attended per call once the stream is warm."""
+    if sc.policy == "convkv":
+        return sc.mem_slots + (sc.window + 1) * sc.tokens_per_block
+    return (sc.static_sink + sc.dyn_topk + sc.window + 1) * sc.tokens_per_block
 
 
 def attn_flops(sc, kv_len):
@@ -64,17 +73,21 @@ def attn_flops(sc, kv_len):
 
 
 def workload_desc(sc, b0, n):
+    if sc.policy == "convkv":
+        cache = (f"ConvKV memory {sc.mem_slots} + window {sc.window} + current = "
+                 f"{context_len(sc)} keys, bf16")
+    else:
+        cache = (f"static sink 1 + pose top-{sc.dyn_topk} + window {sc.window} + current = "
+                 f"{context_len(sc)} keys, K/V {sc.kv_dtype}, {sc.history_mode} history")
     return {
-        "workload": (f"{sc.name}: PR-Sink chunk attention, {sc.num_layers} layers x {sc.n_steps} "
+        "workload": (f"{sc.name}: chunk attention, {sc.num_layers} layers x {sc.n_steps} "
                      f"denoising steps per block, {sc.num_heads} heads x {sc.head_dim}, "
                      f"{sc.tokens_per_block} tokens/block ({sc.frames_per_block}x{sc.grid_h}x"
-                     f"{sc.grid_w}), static sink 1 + pose top-{sc.dyn_topk} + window {sc.window} + "
-                     f"current = {(sc.static_sink + sc.dyn_topk + sc.window + 1) * sc.tokens_per_block}"
-                     f" keys, bf16, external history; stream blocks {b0}..{b0 + n - 1} of "
+                     f"{sc.grid_w}), {cache}; stream blocks {b0}..{b0 + n - 1} of "
                      f"{sc.n_blocks}"),
         "tokens_per_block": sc.tokens_per_block, "heads": sc.num_heads, "head_dim": sc.head_dim,
         "layers": sc.num_layers, "denoise_steps": sc.n_steps, "dyn_topk": sc.dyn_topk,
-        "kv_len": (sc.static_sink + sc.dyn_topk + sc.window + 1) * sc.tokens_per_block,
+        "kv_len": context_len(sc),
         "l2": "inputs larger than L2 (per call: 144 MB Q/K/V, 671 MB attended K/V; L2 126 MB)",
     }
 
@@ -187,6 +200,26 @@ class ClockSampler:
         reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags) if f == "Active"})
         return {"sm_mhz": float(np.median([r[0] for r in rows])),
                 "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_traffic(sc):
+    """DRAM bytes (read + write) per attention launch from the committed ncu
+    summary of this workload, or None when the summary is missing or was
+    taken on a different kernel source (its sha256 is recorded in it)."""
+    import hashlib
+    import re
+    name = {"c3_14b": "attn_tc_kernel_bf16_c3_14b.md", "c5_fp8": "attn_tc_kernel_e4m3_c5_fp8.md"}
+    path = os.path.join(ROOT, "profiles", name.get(sc.name, ""))
+    if not os.path.isfile(path):
+        return None
+    text = open(path).read()
+    src = os.path.join(ROOT, "bounded_kv_cache_la_b300", "csrc", "k_attn_tc.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    m_src = re.search(r"kernel source sha256: ([0-9a-f]{64})", text)
+    m_tr = re.search(r"traffic_bytes_per_launch: (\d+)", text)
+    if not m_src or not m_tr or m_src.group(1) != digest:
+        return None
+    return int(m_tr.group(1))
 
 
 # ------------------------------------------------------------------ extra legs
@@ -360,17 +393,23 @@ def run_ours(a):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
 
-    sc = workload()
+    sc = workload(a.workload)
     if a.layers:
         sc = sc.with_(num_layers=a.layers)
     L, S, T, H, D = sc.num_layers, sc.n_steps, sc.tokens_per_block, sc.num_heads, sc.head_dim
-    # blocks streamed: warm-up, timed, and (e2e leg) one warm-up + e2e_steps
+    external = sc.history_mode == "external"
+    # blocks streamed: warm-up, timed, and (e2e leg) one warm-up + e2e_steps;
+    # an external-history stream resumes late, a resident one (ConvKV) is
+    # streamed from block 0 and is steady once its memory is full
     n_run = a.warmup + a.steps + (0 if a.no_e2e else a.e2e_steps + 1)
-    b0 = max(10, sc.n_blocks - n_run)
+    b0 = max(10, sc.n_blocks - n_run) if external else 10
     kps = gen.poses(sc, n_blocks=b0 + n_run + 1)
 
-    cfg = capi.config_for(sc, max_history=sc.n_blocks + 2)
-    cache = capi.Cache(cfg)
+    cfg = capi.config_for(sc, max_history=b0 + n_run + 2)
+    conv_w = None
+    if sc.policy == "convkv":
+        conv_w = torch.stack([gen.conv_weights_torch(sc, l, "cuda") for l in range(L)]).contiguous()
+    cache = capi.Cache(cfg, conv_w=conv_w)
     g = torch.Generator(device=dev)
     g.manual_seed(1234 + rank)
 
@@ -385,11 +424,12 @@ def run_ours(a):
     # the caller's history store: block id -> bank entry (id mod 4), per layer
     bank = [[(randn(), randn()) for _ in range(4)] for _ in range(L)]
 
-    cache.la_cache_load_history(kps[:b0].reshape(b0, 34))
-    for blk in [0] + list(range(b0 - sc.window, b0)):
-        for l in range(L):
-            kk, vv = bank[l][blk % 4]
-            cache.la_fill_window(l, blk, kk, vv)
+    if external:
+        cache.la_cache_load_history(kps[:b0].reshape(b0, 34))
+        for blk in [0] + list(range(b0 - sc.window, b0)):
+            for l in range(L):
+                kk, vv = bank[l][blk % 4]
+                cache.la_fill_window(l, blk, kk, vv)
 
     qs = [q[l][s] for s in range(S) for l in range(L)]
     ks = [k[l][s] for s in range(S) for l in range(L)]
@@ -401,7 +441,7 @@ def run_ours(a):
         fills["n"] += 1
         return bank[layer][blk % 4]
 
-    state = {"b": b0}
+    state = {"b": 0 if not external else b0}
 
     def step():
         b = state["b"]
@@ -413,6 +453,8 @@ def run_ours(a):
         if world > 1:
             dist.barrier()
 
+    while state["b"] < b0:                      # resident stream: reach steady state
+        step()
     for _ in range(a.warmup):
         step()
     barrier()
@@ -462,7 +504,7 @@ def run_ours(a):
     if st != capi.LA_OK:
         raise RuntimeError(msg)
 
-    ctx_kv = (sc.static_sink + sc.dyn_topk + sc.window + 1) * T
+    ctx_kv = context_len(sc)
     flops_call = attn_flops(sc, ctx_kv)
     flops_block = flops_call * S * L
     t = torch.tensor([elapsed], device=dev)
@@ -475,6 +517,11 @@ def run_ours(a):
     pk, pk_kind = peaks()
     achieved = flops_call / (attn_ms.mean() / 1e3) / 1e12
     peak_sus = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    peak_kind = f"bf16 sustained, {pk_kind}"
+    if sc.kv_dtype == "e4m3":                   # the e4m3 kernel runs kind::f8f6f4
+        f8 = fp8_peak_tflops(torch)
+        if isinstance(f8, float):
+            peak_sus, peak_kind = f8, "e4m3 burst (torch._scaled_mm 8192^3, measured in this run)"
 
     # end to end through the per-call C ABI with pinned host inputs/outputs
     e2e = None
@@ -533,27 +580,25 @@ def run_ours(a):
                       "la_cache_append_block, pinned host Q/K/V in and every output back"}
 
     extra = {}
-    if rank == 0 and not a.no_extra and not a.layers:
+    if rank == 0 and not a.no_extra and not a.layers and a.workload == "c3_14b":
         extra = extra_legs(torch, capi, gen, [x for row in q for x in row],
                            [x for row in k for x in row], [x for row in v for x in row], out, bank,
                            block_ms, peaks()[0])
 
     cpu = None
-    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+    if rank == 0 and world == 1 and not a.no_cpu_baseline and a.workload == "c3_14b":
         smp = OracleSample(workload())
         dt = min(smp.run() for _ in range(2))
         cpu = {"value": smp.flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
                "kind": "oracle", "sample": smp.text, "seconds": dt}
 
     if rank == 0:
-        traffic = None
-        prof_path = os.path.join(ROOT, "profiles", "attn_tc_c3_14b.json")
-        if os.path.exists(prof_path):
-            traffic = json.load(open(prof_path)).get("traffic_bytes_per_launch")
+        traffic = kernel_traffic(sc)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": t_max / a.steps * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3" if sc.kv_dtype == "e4m3" else "bf16",
             "data": "synthetic (seeded torch.randn Q/K/V, synthetic pose stream)",
             "config": workload_desc(sc, b0 + a.warmup, a.steps) | {"parallelism": f"replicas x{world}"},
             "blocks_per_s": blocks_per_s,
@@ -567,7 +612,7 @@ def run_ours(a):
             "fills_per_block": fills_timed / a.steps,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_sus,
                          "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": traffic,
-                         "kernel": "attn_tc_kernel", "peak_kind": f"bf16 sustained, {pk_kind}",
+                         "kernel": "attn_tc_kernel", "peak_kind": peak_kind,
                          "frac_of_burst": achieved / pk["bf16_tflops"]},
             "cpu_baseline": cpu,
             **extra,

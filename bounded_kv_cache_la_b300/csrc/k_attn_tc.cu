@@ -623,109 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   }
 }
 
-// Per-slot rotated copies of the queries: qrot[s][h][t] = R(t0_cur + f - t0_s, row, col) q[t][h].
-// bf16 cache: bf16 copies.  e4m3 cache: e4m3 codes with one fp32 scale per
-// (head, token), qscale[h][t] = m / 448 where m is the largest norm of the
-// token's 64 rotation pairs -- rotations keep pair norms, so one scale
-// serves every slot and no code saturates.  One thread per 8 dims; the 16
-// threads of a (token, head) are 16 consecutive lanes.
-template <bool F8>
-__global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
-  const DevContext& ctx = *a.ctx;
-  const int n_slots = ctx.n_slots;
-  if (n_slots < 1 || n_slots > a.n_qrot) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) record_error(a.err, LA_ERR_DEVICE, KID_QROT, n_slots, a.n_qrot);
-    return;
-  }
-  // every slot's temporal offset must stay inside the RoPE table for every
-  // frame of the block (checked up front so that all threads leave together)
-  for (int s = 0; s < n_slots; ++s) {
-    const int lo = ctx.t0_cur - ctx.t0[s], hi = lo + a.rope.F - 1;
-    if (lo < 0 || hi >= a.rope.max_t) {
-      if (blockIdx.x == 0 && threadIdx.x == 0) record_error(a.err, LA_ERR_DEVICE, KID_QROT, lo, s);
-      return;
-    }
-  }
-  const int chunks = a.D / 8;
-  const long long total = (long long)a.T * a.H * chunks;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  // warp-uniform trip count (the e4m3 path reduces over 16-lane groups)
-  for (long long base = blockIdx.x * (long long)blockDim.x + (threadIdx.x & ~31); base < total;
-       base += stride) {
-    const long long idx = base + (threadIdx.x & 31);
-    const bool valid = idx < total;
-    const long long vi = valid ? idx : 0;
-    const int cch = (int)(vi % chunks);
-    const long long th = vi / chunks;
-    const int h = (int)(th % a.H);
-    const int t = (int)(th / a.H);
-    uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + (size_t)th * a.D + cch * 8);
-    float x[8];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x[2 * e] = __uint_as_float(w[e] << 16);
-      x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-    }
-    float inv = 1.f;
-    if (F8) {
-      float n2 = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) n2 = fmaxf(n2, x[2 * e] * x[2 * e] + x[2 * e + 1] * x[2 * e + 1]);
-#pragma unroll
-      for (int o = 8; o; o >>= 1) n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
-      const float mn = sqrtf(n2);
-      inv = mn > 0.f ? 448.f / mn : 0.f;
-      if (valid && cch == 0) a.qscale[(size_t)h * a.T + t] = mn > 0.f ? mn / 448.f : 1.f;
-    }
-    if (!valid) continue;
-    int f, hh, ww;
-    token_pos(a.rope, t, f, hh, ww);
-    for (int s = 0; s < n_slots; ++s) {
-      const int dtq = ctx.t0_cur + f - ctx.t0[s];
-      float y[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 cs = rope_cs(a.rope, cch * 8 + 2 * e, dtq, hh, ww);
-        const float2 r = rot_exact(x[2 * e], x[2 * e + 1], cs);
-        y[2 * e] = r.x;
-        y[2 * e + 1] = r.y;
-      }
-      const size_t off = (((size_t)s * a.H + h) * a.T + t) * a.D + cch * 8;
-      if (F8) {
-        uint2 o;
-        o.x = cvt_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
-        o.y = cvt_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv);
-        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.qrot) + off) = o;
-      } else {
-        uint4 o;
-        o.x = cvt_bf16x2(y[0], y[1]);
-        o.y = cvt_bf16x2(y[2], y[3]);
-        o.z = cvt_bf16x2(y[4], y[5]);
-        o.w = cvt_bf16x2(y[6], y[7]);
-        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.qrot) + off) = o;
-      }
-    }
-  }
-}
-
 }  // namespace
 
 bool attn_tc_supported(int D, int kv_dtype) {
   return D == kD && (kv_dtype == LA_BF16 || kv_dtype == LA_E4M3);
-}
-
-cudaError_t launch_qrot(const QrotArgs& a, cudaStream_t s) {
-  if (a.D != kD) return cudaErrorInvalidValue;
-  long long work = (long long)a.T * a.H * (a.D / 8);
-  long long grid = (work + 255) / 256;
-  if (grid > 148LL * 16) grid = 148LL * 16;
-  if (a.f8)
-    qrot_kernel<true><<<(int)grid, 256, 0, s>>>(a);
-  else
-    qrot_kernel<false><<<(int)grid, 256, 0, s>>>(a);
-  count_launches(1);
-  return cudaGetLastError();
 }
 
 template <bool F8>

@@ -165,3 +165,65 @@ def test_fp8_14b_shape_sampled_rows():
         return
     o = H.oracle_output(sc, ctx, vals, 0, 0, 1, rows=rows)
     H.compare(outs[9][(0, 0)][rows][:, heads], o, "e4m3_tc", "block 9")
+
+
+def test_convkv_full_shape_sampled_rows():
+    """ConvKV at its full shape (40 heads x 128, 3510 tokens per block,
+    4096-token memory): blocks 9 (memory just saturated: 6 evictions x 702
+    tokens > 4096) and 11, oracle on 3 heads x 192 rows."""
+    sc = C4_CONVKV
+    n = 12
+    keep = {9, 11}
+    _, ctxs, outs = H.run_stream(sc, n, keep, n_steps=1, layers=1, attn_impl=1)
+    heads = [0, 19, 39]
+    vals = H.Values(sc, heads)
+    w = gen.conv_weights_np(sc, 0)[:, heads]
+    rows = np.r_[0:64, 1700:1764, 3446:3510]
+    for b in sorted(keep):
+        ctx = ostream.plan_convkv(sc, b)
+        assert ctxs[b]["mem_tokens"] == ctx.mem_tokens == 4096
+        assert ctxs[b]["kv_len"] == ctx.kv_len == 18136
+        o = H.oracle_output(sc, ctx, vals, 0, 0, 1, rows=rows, w_kv=w)
+        H.compare(outs[b][(0, 0)][rows][:, heads], o, "bf16", f"block {b}")
+
+
+def test_single_ragged_query_tile_odd_heads():
+    """48 tokens per block (one partial query tile per head) and 3 heads:
+    every unit is a half unit; all rows against the oracle."""
+    sc = C2_MID.with_(num_heads=3, frames_per_block=3, grid_h=4, grid_w=4)
+    keep = {0, 3, 4, 6, 9}
+    _, ctxs, outs = H.run_stream(sc, 10, keep, attn_impl=1)
+    ref = ostream.plan_stream(sc, gen.poses(sc, n_blocks=10), 10)
+    vals = H.Values(sc)
+    for b in sorted(keep):
+        ctx = ref[b]
+        assert ctxs[b]["kv_len"] == ctx.kv_len
+        if ctxs[b]["dyn_ids"] != ctx.dyn_ids:
+            assert ctx.gap <= 1e-6
+            continue
+        o = H.oracle_output(sc, ctx, vals, 0, 0, 1)
+        H.compare(outs[b][(0, 0)], o, "bf16", f"block {b}")
+
+
+def test_largest_dynamic_sink():
+    """Top-8 dynamic sink (the most the C ABI takes): 13 slots once warm;
+    ids bit-exact where the gap allows, outputs against the oracle."""
+    sc = C5_FP8.with_(num_heads=2, grid_h=6, grid_w=10, kv_dtype="bf16", dyn_topk=8,
+                      history_mode="resident")                 # 180 tokens per block
+    n = 16
+    keep = {12, 15}
+    _, ctxs, outs = H.run_stream(sc, n, keep, attn_impl=1)
+    ref = ostream.plan_stream(sc, gen.poses(sc, n_blocks=n), n)
+    assert ctxs[15]["n_slots"] == 13 and ctxs[15]["kv_len"] == 13 * sc.tokens_per_block
+    vals = H.Values(sc)
+    for b in range(n):
+        assert ctxs[b]["kv_len"] == ref[b].kv_len
+        if ref[b].gap > 1e-6:
+            assert ctxs[b]["dyn_ids"] == ref[b].dyn_ids
+    for b in sorted(keep):
+        ctx = ref[b]
+        if ctxs[b]["dyn_ids"] != ctx.dyn_ids:
+            assert ctx.gap <= 1e-6
+            continue
+        o = H.oracle_output(sc, ctx, vals, 0, 0, 1)
+        H.compare(outs[b][(0, 0)], o, "bf16", f"block {b}")

@@ -322,7 +322,19 @@ def extra_legs(torch, capi, gen, q, k, v, out, bank, main_block_ms, pk):
     # latency flatness of the 14B stream: blocks 10..12 against the timed blocks
     leg = StreamLeg(torch, capi, gen, C3_14B, 10, 3, q, k, v, out, bank)
     early, _ = leg.time_blocks(3)
+    # static-sink refresh of every layer between two blocks (re-encoded
+    # reference K/V handed in by the caller)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for l in range(C3_14B.num_layers):
+        leg.cache.la_refresh_sink(l, *bank[l % len(bank)][1])
+    e1.record()
+    torch.cuda.synchronize()
+    refresh_ms = e0.elapsed_time(e1)
     leg.close()
+    res["sink_refresh"] = {"layers": C3_14B.num_layers, "ms": refresh_ms,
+                           "note": "la_refresh_sink for every layer of the 14B-shape stream"}
     res["flatness"] = {"c3_14b": {
         "early_blocks": "10-12", "early_block_ms": float(np.median(early)),
         "late_block_ms": float(np.median(main_block_ms)),

@@ -29,7 +29,7 @@ EXPORTS = (
     "la_fill_block", "la_chunk_attention", "la_cache_append_block", "la_stream_step",
     "la_cache_load_history", "la_fill_window", "la_get_error", "la_context_plan",
     "la_debug_page", "la_debug_memory", "la_set_profile_events", "la_launch_count",
-    "la_status_string", "la_pose_topk_noalloc",
+    "la_status_string", "la_pose_topk_noalloc", "la_refresh_sink",
 )
 
 
@@ -114,6 +114,7 @@ def load() -> ctypes.CDLL:
                                  LA_FILL_FN, vp, vp]),
         "la_cache_load_history": (i32, [vp, ctypes.POINTER(ctypes.c_float), i32, vp]),
         "la_fill_window": (i32, [vp, i32, i32, vp, vp, vp]),
+        "la_refresh_sink": (i32, [vp, i32, vp, vp, vp]),
         "la_get_error": (i32, [vp, ctypes.c_char_p, sz]),
         "la_context_plan": (i32, [cfgp, i32, ctypes.POINTER(ctypes.c_int32), i32, ctxp]),
         "la_debug_page": (i32, [vp, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp)]),
@@ -280,6 +281,10 @@ class Cache:
     def la_fill_window(self, layer, block_id, k, v, stream=None):
         _check(self.lib.la_fill_window(self.h, layer, block_id, _ptr(k), _ptr(v),
                                        _stream_handle(stream)), "la_fill_window", self.h)
+
+    def la_refresh_sink(self, layer, k, v, stream=None):
+        _check(self.lib.la_refresh_sink(self.h, layer, _ptr(k), _ptr(v), _stream_handle(stream)),
+               "la_refresh_sink", self.h)
 
     def la_cache_load_history(self, kps, stream=None):
         import numpy as np

@@ -618,6 +618,19 @@ la_status la_fill_window(la_cache_t* c, int layer, int block_id, const void* k, 
   return st;
 }
 
+la_status la_refresh_sink(la_cache_t* c, int layer, const void* k, const void* v, void* stream) {
+  la_status st = check_usable(c);
+  if (st != LA_OK) return st;
+  const auto& g = c->cfg;
+  if (!is_prsink(g) || !g.static_sink) return LA_ERR_UNSUPPORTED;
+  if (layer < 0 || layer >= g.num_layers || !k || !v) return LA_ERR_INVALID_ARG;
+  if (c->selected || c->b < 1 || c->frame_of[0] < 0) return LA_ERR_STATE;
+  const int f = c->frame_of[0];
+  st = write_pages(c, layer, f, k, v, false, static_cast<cudaStream_t>(stream));
+  if (st == LA_OK) c->filled[f][layer] = 1;
+  return st;
+}
+
 la_status la_cache_load_history(la_cache_t* c, const float* kps, int n, void* stream) {
   la_status st = check_usable(c);
   if (st != LA_OK) return st;

@@ -163,6 +163,20 @@ la_status la_chunk_attention(la_cache_t* cache, int layer, const void* q, const 
 la_status la_cache_append_block(la_cache_t* cache, int layer, const void* k, const void* v,
                                 void* stream);
 
+/* Refreshes the static sink of `layer` (PR-Sink with static_sink = 1, once
+ * block 0 has been committed, between blocks): its K/V pages are replaced by
+ * `k`, `v` (device [T][H][D] q_dtype), stored exactly as an appended block
+ * (keys turned by their within-block position, e4m3 with fresh per-head
+ * scales).  The sink keeps its slot and RoPE base.  This is the cache side of
+ * the Rolling Sink Frame Mechanism ("Live Avatar", chatpaper.ai, 摘要 /
+ * abstract): appearance is recalibrated from a cached reference image, i.e.
+ * the caller re-encodes the reference at the current time and hands its K/V
+ * here, at an interval of its choosing.  Returns LA_ERR_UNSUPPORTED for
+ * ConvKV or without a static sink, LA_ERR_STATE inside a block or before
+ * block 0 is committed. */
+la_status la_refresh_sink(la_cache_t* cache, int layer, const void* k, const void* v,
+                          void* stream);
+
 /* Called by la_stream_step for each (layer, block) needing a fill. */
 typedef la_status (*la_fill_fn)(la_cache_t* cache, int layer, int block_id, void* user,
                                 void* stream);

@@ -360,6 +360,20 @@ def extra_legs(torch, capi, gen, q, k, v, out, bank, main_block_ms, pk):
     if isinstance(fp8_pk, float):
         fp8["frac_of_fp8_peak"] = t_fp8 / fp8_pk
     fp8["frac_of_bf16_peak"] = t_fp8 / pk["bf16_tflops"]
+    # the 14B-shape stream itself with an e4m3 cache (top-2, 32760 keys)
+    sc3 = C3_14B.with_(kv_dtype="e4m3")
+    kv3 = context_len(sc3)
+    fl3 = attn_flops(sc3, kv3)
+    leg = StreamLeg(torch, capi, gen, sc3, sc3.n_blocks - 3, 3, q, k, v, out, bank)
+    leg.step()
+    bms, ams = leg.time_blocks(2)
+    leg.close()
+    t3 = fl3 / (np.mean(ams) / 1e3) / 1e12
+    c3f8 = {"kv_len": kv3, "block_ms": float(np.median(bms)), "blocks_per_s": 1e3 / float(np.median(bms)),
+            "attn_call_ms": float(np.mean(ams)), "attn_tflops": t3,
+            "frac_of_bf16_peak": t3 / pk["bf16_tflops"]}
+    if isinstance(fp8_pk, float):
+        c3f8["frac_of_fp8_peak"] = t3 / fp8_pk
     res["flatness"]["c5_fp8"] = {"early_block_ms": fp8["early_block_ms"],
                                  "late_block_ms": fp8["late_block_ms"],
                                  "late_over_early": fp8["late_over_early"]}
@@ -378,6 +392,7 @@ def extra_legs(torch, capi, gen, q, k, v, out, bank, main_block_ms, pk):
     fl4 = attn_flops(sc4, kv4)
     res["variants"] = {
         "c5_fp8": fp8,
+        "c3_14b_e4m3": c3f8,
         "c4_convkv": {"kv_len": kv4, "blocks": "10-12", "block_ms": float(np.median(bms)),
                       "blocks_per_s": 1e3 / float(np.median(bms)),
                       "attn_call_ms": float(np.mean(ams)),

@@ -40,14 +40,15 @@ struct la_cache {
   bool failed = false;
   std::string last_msg;
   la_context ctx{};
-  DevContext dctx{};
+  DevContext dctx{}, dctx_final{};
   std::vector<int> frame_of;        // block -> frame (-1 none)
   std::vector<int> free_frames;
   std::deque<int> window;
   std::vector<int> dyn;
   std::vector<std::vector<char>> filled;   // [frame][layer] pages valid
-  int cur_frame = -1;
+  int cur_frame = -1;               // frame of the block being generated (set at select)
   std::vector<char> appended;
+  std::vector<char> pages_written;  // [layer] the block's pages already hold its final K/V
   float query_kp[34] = {};
   int mem_n = 0, mem_head = 0;      // ConvKV ring state
   bool tc = false;
@@ -147,6 +148,7 @@ void compute_layout(const la_cache_config& c, Layout& L) {
   };
   L.err = take(sizeof(DevError));
   L.ctx = take(sizeof(DevContext));
+  L.ctx_final = take(sizeof(DevContext));
   L.topk = take(sizeof(DevTopk));
   L.amax = take(sizeof(unsigned) * 2 * H);
   L.pose_tab = take(sizeof(float) * 36 * (size_t)hist);
@@ -396,6 +398,7 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
   if (!(is_prsink(*cfg) && !is_external(*cfg)))
     for (int f = L.n_frames - 1; f >= 0; --f) c->free_frames.push_back(f);
   c->appended.assign(cfg->num_layers, 0);
+  c->pages_written.assign(cfg->num_layers, 0);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int dev = 0;
@@ -573,15 +576,40 @@ la_status la_select_context(la_cache_t* c, const float* query_pose, la_context* 
   d.kv_len = ctx.kv_len;
   d.t0_cur = ctx.t0[ctx.n_slots - 1];
   d.block = b;
+
+  // The frame block b will occupy once committed.
+  int fb;
+  if (is_prsink(g) && !is_external(g)) {
+    if (b >= c->L.n_frames) return LA_ERR_OOM;
+    fb = b;
+  } else {
+    fb = alloc_frame(c);
+    if (fb < 0) {
+      c->failed = true;
+      c->last_msg = "no free frame for the block being generated";
+      return LA_ERR_STATE;
+    }
+  }
+  // Same table with the current slot read from that frame: the last
+  // denoising step of la_stream_step writes the block's pages there.
+  DevContext dfin = d;
+  dfin.kind[si - 1] = SLOT_FRAME;
+  dfin.frame[si - 1] = fb;
   c->dctx = d;
+  c->dctx_final = dfin;
   st = cuda_status(c, cudaMemcpyAsync(c->pool + c->L.ctx, &c->dctx, sizeof(d),
                                       cudaMemcpyHostToDevice, s),
                    "upload slot table");
+  if (st == LA_OK)
+    st = cuda_status(c, cudaMemcpyAsync(c->pool + c->L.ctx_final, &c->dctx_final, sizeof(d),
+                                        cudaMemcpyHostToDevice, s),
+                     "upload slot table");
   if (st != LA_OK) return st;
   c->ctx = ctx;
   c->selected = true;
-  c->cur_frame = -1;
+  c->cur_frame = fb;
   std::fill(c->appended.begin(), c->appended.end(), 0);
+  std::fill(c->pages_written.begin(), c->pages_written.end(), 0);
   if (out) *out = ctx;
   return LA_OK;
 }
@@ -667,24 +695,40 @@ la_status la_cache_load_history(la_cache_t* c, const float* kps, int n, void* st
   return LA_OK;
 }
 
-la_status la_chunk_attention(la_cache_t* c, int layer, const void* q, const void* k_cur,
-                             const void* v_cur, void* out, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// One chunk attention.  final = the last denoising step of the block inside
+// la_stream_step: k_cur / v_cur are then also the block's final K/V, so they
+// are written straight into the block's own frame (the slot table whose
+// current slot is that frame is used) and the layer's append skips its copy.
+la_status chunk_attention(la_cache* c, int layer, const void* q, const void* k_cur,
+                          const void* v_cur, void* out, cudaStream_t s, bool final) {
   la_status st = check_usable(c);
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
   if (!c->selected) return LA_ERR_STATE;
   if (layer < 0 || layer >= g.num_layers || !q || !k_cur || !v_cur || !out)
     return LA_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (final && c->appended[layer]) return LA_ERR_STATE;
   if (is_prsink(g) && is_external(g)) {
     for (int e = 0; e < c->ctx.n_slots - 1; ++e) {
       int f = c->frame_of[c->ctx.block_id[e]];
       if (f < 0 || !c->filled[f][layer]) return LA_ERR_STATE;
     }
   }
-  st = write_pages(c, layer, -1, k_cur, v_cur, false, s);
-  if (st != LA_OK) return st;
-  const DevContext* dctx = reinterpret_cast<const DevContext*>(c->pool + c->L.ctx);
+  if (final) {
+    st = write_pages(c, layer, c->cur_frame, k_cur, v_cur, !is_prsink(g), s);
+    if (st != LA_OK) return st;
+    c->filled[c->cur_frame][layer] = 1;
+    c->pages_written[layer] = 1;
+  } else {
+    st = write_pages(c, layer, -1, k_cur, v_cur, false, s);
+    if (st != LA_OK) return st;
+  }
+  const DevContext* dctx =
+      reinterpret_cast<const DevContext*>(c->pool + (final ? c->L.ctx_final : c->L.ctx));
   DevError* err = reinterpret_cast<DevError*>(c->pool + c->L.err);
   if (c->tc) {
     QrotArgs qa{};
@@ -756,6 +800,15 @@ la_status la_chunk_attention(la_cache_t* c, int layer, const void* q, const void
   return st;
 }
 
+}  // namespace
+
+extern "C" {
+
+la_status la_chunk_attention(la_cache_t* c, int layer, const void* q, const void* k_cur,
+                             const void* v_cur, void* out, void* stream) {
+  return chunk_attention(c, layer, q, k_cur, v_cur, out, static_cast<cudaStream_t>(stream), false);
+}
+
 la_status la_cache_append_block(la_cache_t* c, int layer, const void* k, const void* v,
                                 void* stream) {
   la_status st = check_usable(c);
@@ -766,25 +819,13 @@ la_status la_cache_append_block(la_cache_t* c, int layer, const void* k, const v
   if (c->appended[layer]) return LA_ERR_STATE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int b = c->b;
-  if (c->cur_frame < 0) {
-    int f;
-    if (is_prsink(g) && !is_external(g)) {
-      if (b >= c->L.n_frames) return LA_ERR_OOM;
-      f = b;
-    } else {
-      f = alloc_frame(c);
-      if (f < 0) {
-        c->failed = true;
-        c->last_msg = "no free frame for the appended block";
-        return LA_ERR_STATE;
-      }
-    }
-    c->cur_frame = f;
-  }
+  if (c->cur_frame < 0) return LA_ERR_STATE;
   const bool convkv = !is_prsink(g);
-  st = write_pages(c, layer, c->cur_frame, k, v, convkv, s);
-  if (st != LA_OK) return st;
-  c->filled[c->cur_frame][layer] = 1;
+  if (!c->pages_written[layer]) {
+    st = write_pages(c, layer, c->cur_frame, k, v, convkv, s);
+    if (st != LA_OK) return st;
+    c->filled[c->cur_frame][layer] = 1;
+  }
 
   if (convkv && (int)c->window.size() == g.window) {
     // The oldest exact block leaves the window: compress it into the memory.
@@ -870,7 +911,8 @@ la_status la_stream_step(la_cache_t* c, const float* pose, int n_steps, const vo
   for (int sidx = 0; sidx < n_steps; ++sidx)
     for (int l = 0; l < L; ++l) {
       size_t i = (size_t)sidx * L + l;
-      st = la_chunk_attention(c, l, q[i], k[i], v[i], out[i], stream);
+      st = chunk_attention(c, l, q[i], k[i], v[i], out[i], static_cast<cudaStream_t>(stream),
+                           sidx == n_steps - 1);
       if (st != LA_OK) return st;
     }
   for (int l = 0; l < L; ++l) {

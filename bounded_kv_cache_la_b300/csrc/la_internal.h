@@ -53,6 +53,7 @@ struct DevTopk {
 // Byte offsets of every region inside the caller's pool.
 struct Layout {
   size_t err, ctx, topk;           // control
+  size_t ctx_final;                // slot table whose current slot is the block's own frame
   size_t amax;                     // e4m3 amax scratch [2][H] uint32
   size_t pose_tab;                 // [max_history][36] fp32
   size_t inv_norm;                 // [max_history] fp32

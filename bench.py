@@ -314,6 +314,78 @@ class StreamLeg:
         self.cache.close()
 
 
+def host_tier_leg(torch, capi, gen, q, k, v, out, bank, ahead, n_time=3):
+    """The 14B-shape stream with its history tier in page-locked host memory:
+    retrieved blocks are copied host -> device by the copy engines and then
+    written into the cache by la_fill_block, either at select on the compute
+    stream, or -- ahead=True -- fetched during the previous block
+    (la_prefetch_context) on a copy stream.  Returns the median ms per block."""
+    from synth import C3_14B
+    sc = C3_14B
+    L, S = sc.num_layers, sc.n_steps
+    b0 = sc.n_blocks - n_time - 2
+    kps = gen.poses(sc, n_blocks=sc.n_blocks + 1)
+    cache = capi.Cache(capi.config_for(sc, max_history=sc.n_blocks + 2))
+    cache.la_cache_load_history(kps[:b0].reshape(b0, 34))
+    for blk in [0] + list(range(b0 - sc.window, b0)):
+        for l in range(L):
+            cache.la_fill_window(l, blk, *bank[l][blk % 4])
+    hbank = [(bank[0][i][0].cpu().pin_memory(), bank[0][i][1].cpu().pin_memory()) for i in range(4)]
+    # device staging for one block's picks: the copy engines move host -> device,
+    # then the fill kernel (rotation, layout) runs from device memory
+    stage = [[(torch.empty_like(bank[0][0][0]), torch.empty_like(bank[0][0][1])) for _ in range(L)]
+             for _ in range(C3_14B.dyn_topk)]
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    n = len(q)
+
+    def fill_from_host(picks, stream):
+        for i, (blk, need) in enumerate(picks):
+            if not need:
+                continue
+            for l in range(L):
+                sk, sv = stage[i][l]
+                sk.copy_(hbank[blk % 4][0], non_blocking=True)
+                sv.copy_(hbank[blk % 4][1], non_blocking=True)
+                cache.la_fill_block(l, blk, sk, sv, stream=stream)
+
+    def block(b):
+        ctx = cache.la_select_context(kps[b])
+        fill_from_host(list(zip(ctx["dyn_ids"], ctx["need_fill"])), main)
+        ev = None
+        if ahead:
+            nxt = cache.la_prefetch_context(kps[b + 1])
+            with torch.cuda.stream(side):
+                side.wait_stream(main)
+                fill_from_host(list(zip(nxt["dyn_ids"], nxt["need_fill"])), side)
+                ev = torch.cuda.Event()
+                ev.record(side)
+        for s_ in range(S):
+            for l in range(L):
+                i = (b + s_ * L + l) % n
+                cache.la_chunk_attention(l, q[i], k[i], v[i], out[l % len(out)])
+        for l in range(L):
+            i = (b + (S - 1) * L + l) % n
+            cache.la_cache_append_block(l, k[i], v[i])
+        if ev is not None:
+            main.wait_event(ev)
+
+    block(b0)
+    block(b0 + 1)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_time + 1)]
+    torch.cuda.synchronize()
+    marks[0].record()
+    for t in range(n_time):
+        block(b0 + 2 + t)
+        marks[t + 1].record()
+    torch.cuda.synchronize()
+    st, msg = cache.la_get_error()
+    if st != capi.LA_OK:
+        raise RuntimeError(msg)
+    cache.close()
+    return float(np.median([marks[t].elapsed_time(marks[t + 1]) for t in range(n_time)]))
+
+
 def extra_legs(torch, capi, gen, q, k, v, out, bank, main_block_ms, pk):
     """FP8 stress stream, ConvKV stream and the latency-flatness check."""
     from synth import C3_14B, C4_CONVKV, C5_FP8
@@ -390,6 +462,13 @@ def extra_legs(torch, capi, gen, q, k, v, out, bank, main_block_ms, pk):
     leg.close()
     kv4 = sc4.mem_slots + (sc4.window + 1) * T4
     fl4 = attn_flops(sc4, kv4)
+    at_select = host_tier_leg(torch, capi, gen, q, k, v, out, bank, ahead=False)
+    fetched = host_tier_leg(torch, capi, gen, q, k, v, out, bank, ahead=True)
+    res["host_history_tier"] = {
+        "note": "14B stream, retrieved blocks copied from page-locked host memory (2 blocks x 40 "
+                "layers x 96 MB per block) then filled; device-memory history = the main leg",
+        "fills_at_select_block_ms": at_select, "fetched_ahead_block_ms": fetched,
+        "device_history_block_ms": float(np.median(main_block_ms))}
     res["variants"] = {
         "c5_fp8": fp8,
         "c3_14b_e4m3": c3f8,

@@ -29,7 +29,7 @@ EXPORTS = (
     "la_fill_block", "la_chunk_attention", "la_cache_append_block", "la_stream_step",
     "la_cache_load_history", "la_fill_window", "la_get_error", "la_context_plan",
     "la_debug_page", "la_debug_memory", "la_set_profile_events", "la_launch_count",
-    "la_status_string", "la_pose_topk_noalloc", "la_refresh_sink",
+    "la_status_string", "la_pose_topk_noalloc", "la_refresh_sink", "la_prefetch_context",
 )
 
 
@@ -115,6 +115,7 @@ def load() -> ctypes.CDLL:
         "la_cache_load_history": (i32, [vp, ctypes.POINTER(ctypes.c_float), i32, vp]),
         "la_fill_window": (i32, [vp, i32, i32, vp, vp, vp]),
         "la_refresh_sink": (i32, [vp, i32, vp, vp, vp]),
+        "la_prefetch_context": (i32, [vp, ctypes.POINTER(ctypes.c_float), ctxp, vp]),
         "la_get_error": (i32, [vp, ctypes.c_char_p, sz]),
         "la_context_plan": (i32, [cfgp, i32, ctypes.POINTER(ctypes.c_int32), i32, ctxp]),
         "la_debug_page": (i32, [vp, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp)]),
@@ -263,6 +264,15 @@ class Cache:
         out = la_context()
         _check(self.lib.la_select_context(self.h, kp, ctypes.byref(out), _stream_handle(stream)),
                "la_select_context", self.h)
+        return out.as_dict()
+
+    def la_prefetch_context(self, next_pose, stream=None) -> dict:
+        import numpy as np
+        arr = np.ascontiguousarray(np.asarray(next_pose, dtype=np.float32).reshape(34))
+        out = la_context()
+        _check(self.lib.la_prefetch_context(self.h, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                            ctypes.byref(out), _stream_handle(stream)),
+               "la_prefetch_context", self.h)
         return out.as_dict()
 
     def la_chunk_attention(self, layer, q, k, v, out, stream=None):

@@ -45,6 +45,8 @@ struct la_cache {
   std::vector<int> free_frames;
   std::deque<int> window;
   std::vector<int> dyn;
+  std::vector<int> pre;             // dynamic sink fetched ahead for block pre_for
+  int pre_for = -1;
   std::vector<std::vector<char>> filled;   // [frame][layer] pages valid
   int cur_frame = -1;               // frame of the block being generated (set at select)
   std::vector<char> appended;
@@ -129,7 +131,9 @@ void compute_layout(const la_cache_config& c, Layout& L) {
   L.T = T;
   L.G = is_prsink(c) ? 2 : 3;
   if (is_prsink(c))
-    L.n_frames = is_external(c) ? c.static_sink + c.window + 1 + c.dyn_topk : c.max_history;
+    // EXTERNAL: sink + window + current + dynamic sink, and as many again for
+    // the next block's dynamic sink fetched ahead (la_prefetch_context)
+    L.n_frames = is_external(c) ? c.static_sink + c.window + 1 + 2 * c.dyn_topk : c.max_history;
   else
     L.n_frames = c.window + 1;
   const int S = exact_slots(c);
@@ -150,7 +154,10 @@ void compute_layout(const la_cache_config& c, Layout& L) {
   L.ctx = take(sizeof(DevContext));
   L.ctx_final = take(sizeof(DevContext));
   L.topk = take(sizeof(DevTopk));
-  L.amax = take(sizeof(unsigned) * 2 * H);
+  // e4m3 amax scratch, one [2][H] slice per frame plus one for the current
+  // pages, so page writes to different frames may run on different streams
+  L.amax = take(c.kv_dtype == LA_E4M3 ? sizeof(unsigned) * 2 * H * ((size_t)L.n_frames + 1)
+                                      : sizeof(unsigned) * 2 * H);
   L.pose_tab = take(sizeof(float) * 36 * (size_t)hist);
   L.inv_norm = take(sizeof(float) * (size_t)hist);
   L.scores = take(sizeof(float) * (size_t)hist);
@@ -227,7 +234,8 @@ la_status write_pages(la_cache* c, int layer, int frame, const void* k, const vo
     a.k_scale = reinterpret_cast<float*>(c->pool + c->L.cur_scales);
     a.v_scale = a.k_scale + g.num_heads;
   }
-  a.amax = reinterpret_cast<unsigned*>(c->pool + c->L.amax);
+  a.amax = reinterpret_cast<unsigned*>(c->pool + c->L.amax) +
+           (g.kv_dtype == LA_E4M3 ? (size_t)(frame >= 0 ? frame : c->L.n_frames) * 2 * g.num_heads : 0);
   a.T = c->T;
   a.H = g.num_heads;
   a.D = g.head_dim;
@@ -302,6 +310,61 @@ bool encode_map(la_cache* c, CUtensorMap* m, void* base, int d, uint64_t rows_pe
   (void)c;
   return r == CUDA_SUCCESS;
 }
+
+// Pose retrieval for block `blk` (query pose `kp`, written to table row
+// blk): the top-k candidates (ids ascending, their scores) and the k-th /
+// (k+1)-th score gap.  Synchronises `s` to read the picks.
+la_status retrieve(la_cache* c, const float* kp, int blk, std::vector<int>& ids,
+                   std::vector<float>& scores, float& gap, cudaStream_t s) {
+  const auto& g = c->cfg;
+  RetrievalArgs a{};
+  std::memcpy(a.kp, kp, sizeof(a.kp));
+  a.pose_row = blk;
+  a.c0 = g.static_sink ? 1 : 0;
+  a.c1 = std::max(a.c0, blk - g.window);
+  a.k = g.dyn_topk;
+  a.max_history = g.max_history;
+  a.table = reinterpret_cast<float*>(c->pool + c->L.pose_tab);
+  a.inv_norm = reinterpret_cast<float*>(c->pool + c->L.inv_norm);
+  a.scores = reinterpret_cast<float*>(c->pool + c->L.scores);
+  a.topk = reinterpret_cast<DevTopk*>(c->pool + c->L.topk);
+  a.err = reinterpret_cast<DevError*>(c->pool + c->L.err);
+  la_status st = cuda_status(c, launch_retrieval(a, s), "retrieval kernel");
+  if (st != LA_OK) return st;
+  DevError e{};
+  DevTopk tk{};
+  st = cuda_status(c, cudaMemcpyAsync(&tk, a.topk, sizeof(tk), cudaMemcpyDeviceToHost, s),
+                   "read retrieval");
+  if (st == LA_OK)
+    st = cuda_status(c, cudaMemcpyAsync(&e, a.err, sizeof(DevError), cudaMemcpyDeviceToHost, s),
+                     "read error word");
+  if (st == LA_OK) st = cuda_status(c, cudaStreamSynchronize(s), "retrieval sync");
+  if (st != LA_OK) return st;
+  if (e.code != 0) {
+    c->failed = true;
+    return (la_status)e.code;
+  }
+  const int n = std::min(tk.n, g.dyn_topk);
+  std::vector<std::pair<int, float>> picks;
+  for (int i = 0; i < n; ++i) picks.push_back({tk.ids[i], tk.scores[i]});
+  gap = INFINITY;
+  if (tk.n > g.dyn_topk && g.dyn_topk > 0) gap = tk.scores[g.dyn_topk - 1] - tk.scores[g.dyn_topk];
+  std::sort(picks.begin(), picks.end());
+  ids.clear();
+  scores.clear();
+  for (auto& p : picks) {
+    if (p.first < a.c0 || p.first >= a.c1) {
+      c->failed = true;
+      c->last_msg = "retrieval returned a non-candidate id";
+      return LA_ERR_DEVICE;
+    }
+    ids.push_back(p.first);
+    scores.push_back(p.second);
+  }
+  return LA_OK;
+}
+
+bool contains(const std::vector<int>& v, int x) { return std::find(v.begin(), v.end(), x) != v.end(); }
 
 la_status check_usable(la_cache* c) {
   if (!c) return LA_ERR_INVALID_ARG;
@@ -476,49 +539,11 @@ la_status la_select_context(la_cache_t* c, const float* query_pose, la_context* 
       if (c->frame_of[0] < 0) return LA_ERR_STATE;
       sink.push_back(0);
     }
-    RetrievalArgs a{};
-    std::memcpy(a.kp, query_pose, sizeof(a.kp));
-    std::memcpy(c->query_kp, query_pose, sizeof(a.kp));
-    a.pose_row = b;
-    a.c0 = g.static_sink ? 1 : 0;
-    a.c1 = std::max(a.c0, b - g.window);
-    a.k = g.dyn_topk;
-    a.max_history = g.max_history;
-    a.table = reinterpret_cast<float*>(c->pool + c->L.pose_tab);
-    a.inv_norm = reinterpret_cast<float*>(c->pool + c->L.inv_norm);
-    a.scores = reinterpret_cast<float*>(c->pool + c->L.scores);
-    a.topk = reinterpret_cast<DevTopk*>(c->pool + c->L.topk);
-    a.err = reinterpret_cast<DevError*>(c->pool + c->L.err);
-    st = cuda_status(c, launch_retrieval(a, s), "retrieval kernel");
+    std::memcpy(c->query_kp, query_pose, sizeof(c->query_kp));
+    std::vector<float> scores;
+    st = retrieve(c, query_pose, b, dyn, scores, gap, s);
     if (st != LA_OK) return st;
-    struct { DevError e; } eh{};
-    DevTopk tk{};
-    st = cuda_status(c, cudaMemcpyAsync(&tk, a.topk, sizeof(tk), cudaMemcpyDeviceToHost, s),
-                     "read retrieval");
-    if (st == LA_OK)
-      st = cuda_status(c, cudaMemcpyAsync(&eh.e, a.err, sizeof(DevError), cudaMemcpyDeviceToHost, s),
-                       "read error word");
-    if (st == LA_OK) st = cuda_status(c, cudaStreamSynchronize(s), "retrieval sync");
-    if (st != LA_OK) return st;
-    if (eh.e.code != 0) {
-      c->failed = true;
-      return (la_status)eh.e.code;
-    }
-    const int n = std::min(tk.n, g.dyn_topk);
-    std::vector<std::pair<int, float>> picks;
-    for (int i = 0; i < n; ++i) picks.push_back({tk.ids[i], tk.scores[i]});
-    if (tk.n > g.dyn_topk && g.dyn_topk > 0)
-      gap = tk.scores[g.dyn_topk - 1] - tk.scores[g.dyn_topk];
-    std::sort(picks.begin(), picks.end());
-    for (auto& p : picks) {
-      if (p.first < a.c0 || p.first >= a.c1) {
-        c->failed = true;
-        c->last_msg = "retrieval returned a non-candidate id";
-        return LA_ERR_DEVICE;
-      }
-      dyn.push_back(p.first);
-      dyn_scores.push_back(p.second);
-    }
+    dyn_scores = scores;
   }
 
   int mem_n = is_prsink(g) ? 0 : c->mem_n;
@@ -527,10 +552,17 @@ la_status la_select_context(la_cache_t* c, const float* query_pose, la_context* 
   ctx.topk_gap = gap;
   for (size_t i = 0; i < dyn_scores.size(); ++i) ctx.dyn_scores[i] = dyn_scores[i];
 
-  // Dynamic-sink frames.
+  // Dynamic-sink frames.  Blocks of the previous dynamic sink, or fetched
+  // ahead for this block, that are not picked now (and are not the sink or
+  // in the window) give their frames back.
   if (is_prsink(g) && is_external(g)) {
-    for (int id : c->dyn)
-      if (std::find(dyn.begin(), dyn.end(), id) == dyn.end()) release_frame(c, id);
+    std::vector<int> old = c->dyn;
+    if (c->pre_for == b) old.insert(old.end(), c->pre.begin(), c->pre.end());
+    for (int id : old)
+      if (!contains(dyn, id) && !contains(win, id) && !(g.static_sink && id == 0))
+        release_frame(c, id);
+    c->pre.clear();
+    c->pre_for = -1;
     for (size_t i = 0; i < dyn.size(); ++i) {
       int id = dyn[i];
       if (c->frame_of[id] < 0) {
@@ -620,13 +652,58 @@ la_status la_fill_block(la_cache_t* c, int layer, int block_id, const void* k, c
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
   if (!is_prsink(g) || !is_external(g)) return LA_ERR_UNSUPPORTED;
-  if (!c->selected) return LA_ERR_STATE;
   if (layer < 0 || layer >= g.num_layers || !k || !v) return LA_ERR_INVALID_ARG;
-  if (std::find(c->dyn.begin(), c->dyn.end(), block_id) == c->dyn.end()) return LA_ERR_INVALID_ARG;
+  const bool cur = c->selected && contains(c->dyn, block_id);
+  const bool ahead = c->pre_for >= c->b && contains(c->pre, block_id);
+  if (!cur && !ahead) return c->selected || c->pre_for >= c->b ? LA_ERR_INVALID_ARG : LA_ERR_STATE;
   int f = c->frame_of[block_id];
+  if (f < 0) return LA_ERR_STATE;
   st = write_pages(c, layer, f, k, v, false, static_cast<cudaStream_t>(stream));
   if (st == LA_OK) c->filled[f][layer] = 1;
   return st;
+}
+
+la_status la_prefetch_context(la_cache_t* c, const float* next_pose, la_context* out,
+                              void* stream) {
+  la_status st = check_usable(c);
+  if (st != LA_OK) return st;
+  const auto& g = c->cfg;
+  if (!is_prsink(g) || !is_external(g)) return LA_ERR_UNSUPPORTED;
+  if (!c->selected || c->pre_for == c->b + 1) return LA_ERR_STATE;
+  if (!next_pose) return LA_ERR_INVALID_ARG;
+  for (int i = 0; i < 34; ++i)
+    if (!std::isfinite(next_pose[i])) return LA_ERR_INVALID_ARG;
+  const int b1 = c->b + 1;
+  if (b1 >= g.max_history) return LA_ERR_OOM;
+  std::vector<int> ids;
+  std::vector<float> scores;
+  float gap = INFINITY;
+  st = retrieve(c, next_pose, b1, ids, scores, gap, static_cast<cudaStream_t>(stream));
+  if (st != LA_OK) return st;
+  la_context ctx;
+  std::vector<int> sink;
+  if (g.static_sink) sink.push_back(0);
+  plan_slots(g, b1, sink, ids, window_blocks(g, b1), 0, &ctx);
+  ctx.topk_gap = gap;
+  for (size_t i = 0; i < ids.size(); ++i) {
+    const int id = ids[i];
+    if (c->frame_of[id] < 0) {
+      const int f = alloc_frame(c);
+      if (f < 0) {
+        c->failed = true;
+        c->last_msg = "no free frame for a block fetched ahead";
+        return LA_ERR_STATE;
+      }
+      c->frame_of[id] = f;
+    }
+    const int f = c->frame_of[id];
+    ctx.dyn_scores[i] = scores[i];
+    ctx.need_fill[i] = std::all_of(c->filled[f].begin(), c->filled[f].end(), [](char x) { return x; }) ? 0 : 1;
+  }
+  c->pre = ids;
+  c->pre_for = b1;
+  if (out) *out = ctx;
+  return LA_OK;
 }
 
 la_status la_fill_window(la_cache_t* c, int layer, int block_id, const void* k, const void* v,
@@ -871,7 +948,9 @@ la_status la_cache_append_block(la_cache_t* c, int layer, const void* k, const v
     if ((int)c->window.size() > g.window) {
       const int e = c->window.front();
       c->window.pop_front();
-      if (!(is_prsink(g) && !is_external(g))) release_frame(c, e);
+      // EXTERNAL: a block fetched ahead for the next block keeps its frame
+      const bool ahead = is_external(g) && c->pre_for == b + 1 && contains(c->pre, e);
+      if (!(is_prsink(g) && !is_external(g)) && !ahead) release_frame(c, e);
       if (convkv) {
         const int n_out = (c->T - g.conv_kernel) / g.conv_stride + 1;
         const int total = c->mem_n + n_out;

@@ -136,11 +136,28 @@ la_status la_select_context(la_cache_t* cache, const float* query_pose, la_conte
                             void* stream);
 
 /* EXTERNAL history only: writes the K/V of history block `block_id` for
- * `layer` into the dynamic-sink page the last la_select_context gave it
- * (need_fill = 1).  k, v: device [T][H][D] q_dtype, the block's final K/V as
- * la_cache_append_block received them. */
+ * `layer` into the dynamic-sink page the last la_select_context (or
+ * la_prefetch_context) gave it (need_fill = 1).  k, v: [T][H][D] q_dtype,
+ * the block's final K/V as la_cache_append_block received them, in device
+ * memory or in page-locked host memory the device can address (the kernel
+ * then reads it over the bus: a host-memory history tier). */
 la_status la_fill_block(la_cache_t* cache, int layer, int block_id, const void* k,
                         const void* v, void* stream);
+
+/* EXTERNAL history only, while block b is in progress (after its
+ * la_select_context): runs the pose retrieval of block b + 1 for
+ * `next_pose` (host, 17 (x, y) keypoints) -- its candidates are all
+ * committed already -- and reserves a page for every picked block not in
+ * the pool.  `out` (host, optional) gets block b + 1's context; need_fill
+ * marks the picks whose K/V must be written with la_fill_block (on any
+ * stream, e.g. a copy stream, so the writes overlap block b's attention;
+ * the caller orders them before block b + 1's first attention).  A later
+ * la_select_context for block b + 1 with the same pose finds those blocks
+ * in place.  This is the "block offload" deployment the LiveAct page names
+ * (上手实践指南: 显存块卸载), with the next block's pose known ahead.  One
+ * call per block; LA_ERR_STATE outside a block. */
+la_status la_prefetch_context(la_cache_t* cache, const float* next_pose, la_context* out,
+                              void* stream);
 
 /* Block-causal chunk attention of the current block for one layer
  * ([LA] 方法): every query token of the block attends, without mask, to all

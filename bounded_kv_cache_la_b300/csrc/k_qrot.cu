@@ -76,17 +76,48 @@ __global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
     if (!valid) continue;
     int f, hh, ww;
     token_pos(a.rope, t, f, hh, ww);
-    for (int s = 0; s < n_slots; ++s) {
-      const int dtq = ctx.t0_cur + f - ctx.t0[s];
-      float y[8];
+    // Pairs in the height / width parts turn the same way for every slot:
+    // rotate them once.  Only temporal pairs (dims < dt) depend on the slot.
+    const int d0 = cch * 8;
+    float y[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 cs = rope_cs(a.rope, cch * 8 + 2 * e, dtq, hh, ww);
-        const float2 r = rot_exact(x[2 * e], x[2 * e + 1], cs);
+    for (int e = 0; e < 4; ++e) {
+      if (d0 + 2 * e >= a.rope.dt) {
+        const float2 r = rot_exact(x[2 * e], x[2 * e + 1], rope_cs(a.rope, d0 + 2 * e, 0, hh, ww));
         y[2 * e] = r.x;
         y[2 * e + 1] = r.y;
       }
-      const size_t off = (((size_t)s * a.H + h) * a.T + t) * a.D + cch * 8;
+    }
+    const bool temporal = d0 < a.rope.dt;
+    uint4 fixed_bf16{};
+    uint2 fixed_f8{};
+    if (!temporal) {
+      if (F8) {
+        fixed_f8.x = cvt_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
+        fixed_f8.y = cvt_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv);
+      } else {
+        fixed_bf16 = make_uint4(cvt_bf16x2(y[0], y[1]), cvt_bf16x2(y[2], y[3]), cvt_bf16x2(y[4], y[5]),
+                                cvt_bf16x2(y[6], y[7]));
+      }
+    }
+    for (int s = 0; s < n_slots; ++s) {
+      const size_t off = (((size_t)s * a.H + h) * a.T + t) * a.D + d0;
+      if (!temporal) {
+        if (F8)
+          *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.qrot) + off) = fixed_f8;
+        else
+          *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.qrot) + off) = fixed_bf16;
+        continue;
+      }
+      const int dtq = ctx.t0_cur + f - ctx.t0[s];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (d0 + 2 * e < a.rope.dt) {
+          const float2 r = rot_exact(x[2 * e], x[2 * e + 1], a.rope.tab_t[dtq * (a.rope.dt >> 1) + ((d0 + 2 * e) >> 1)]);
+          y[2 * e] = r.x;
+          y[2 * e + 1] = r.y;
+        }
+      }
       if (F8) {
         uint2 o;
         o.x = cvt_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);

@@ -30,7 +30,9 @@ EXPORTS = (
     "la_cache_load_history", "la_fill_window", "la_get_error", "la_context_plan",
     "la_debug_page", "la_debug_memory", "la_set_profile_events", "la_launch_count",
     "la_status_string", "la_pose_topk_noalloc", "la_refresh_sink", "la_prefetch_context",
+    "la_debug_inject",
 )
+LA_INJECT_ATTN_STALL = 1
 
 
 class la_cache_config(ctypes.Structure):
@@ -116,6 +118,7 @@ def load() -> ctypes.CDLL:
         "la_fill_window": (i32, [vp, i32, i32, vp, vp, vp]),
         "la_refresh_sink": (i32, [vp, i32, vp, vp, vp]),
         "la_prefetch_context": (i32, [vp, ctypes.POINTER(ctypes.c_float), ctxp, vp]),
+        "la_debug_inject": (i32, [vp, i32, i32]),
         "la_get_error": (i32, [vp, ctypes.c_char_p, sz]),
         "la_context_plan": (i32, [cfgp, i32, ctypes.POINTER(ctypes.c_int32), i32, ctxp]),
         "la_debug_page": (i32, [vp, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp)]),
@@ -343,6 +346,9 @@ class Cache:
                                         ctypes.byref(r), ctypes.byref(n), ctypes.byref(o)),
                "la_debug_memory")
         return k.value, v.value, r.value, n.value, o.value
+
+    def la_debug_inject(self, what, count):
+        _check(self.lib.la_debug_inject(self.h, what, count), "la_debug_inject")
 
     def la_set_profile_events(self, starts, stops):
         """starts/stops: sequences of raw cudaEvent_t handles (ints)."""

@@ -44,8 +44,9 @@
 // and 2^n added to the exponent bits.  P is rounded to bf16 (relative error
 // 2^-9) before the PV product either way.
 //
-// Every wait is bounded (2 s); on timeout the kernel latches LA_ERR_TIMEOUT,
-// drains its in-flight copies and MMAs, frees TMEM and returns.
+// Every wait is bounded (2 s, or the injected limit); on timeout the kernel
+// latches LA_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM
+// and returns.
 #include "dev_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -61,7 +62,6 @@ constexpr int kD = 128;                  // head dim
 constexpr int kKSt = 2, kVSt = 2;
 constexpr int kThreads = 384;
 constexpr int kCtlBytes = 1024;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 // Register split: launched at 168 per thread (384 threads, 1 CTA per SM =
 // 64512).  Control warpgroup 128 x 88 + two softmax warpgroups 2 x 128 x 208
 // = 64512.
@@ -107,6 +107,7 @@ struct Ctl {
   uint64_t v_full[kVSt], v_empty[kVSt];
   uint64_t s_full[2], p_ready[2], o_full[2];
   uint64_t mma_done;
+  uint64_t never;                  // failure injection: nothing arrives here
   uint32_t tmem_base;
   int abort_flag;
   DevContext ctx;
@@ -116,6 +117,7 @@ static_assert(sizeof(Ctl) <= kCtlBytes, "control block too large");
 struct Wait {
   volatile int* abort_flag;
   DevError* err;
+  uint64_t timeout_ns;
   __device__ __forceinline__ bool operator()(const uint64_t& bar, uint32_t parity, int where) const {
     const uint32_t b = smem_u32(&bar);
     if (mbar_try_wait(b, parity)) return true;
@@ -124,7 +126,7 @@ struct Wait {
       if (mbar_try_wait(b, parity)) return true;
       if ((it & 31) == 0) {
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
+        if (globaltimer() - t0 > timeout_ns) {
           *abort_flag = 1;
           record_error(err, LA_ERR_TIMEOUT, KID_ATTN_TC, where, blockIdx.x);
           return false;
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       mbar_init(smem_u32(&ctl.o_full[i]), 1);
     }
     mbar_init(smem_u32(&ctl.mma_done), 1);
+    mbar_init(smem_u32(&ctl.never), 1);
     ctl.abort_flag = 0;
     ctl.ctx = *a.ctx;
     fence_barrier_init();
@@ -259,7 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           (k == SLOT_FRAME && (cx.frame[s] < 0 || cx.frame[s] >= a.n_frames)) ||
           (k != SLOT_MEMORY && tok > a.T) || (F8 && k == SLOT_MEMORY);
   }
-  const Wait wait{&ctl.abort_flag, a.err};
+  const Wait wait{&ctl.abort_flag, a.err, a.timeout_ns};
+  const uint64_t limit_ns = a.timeout_ns;
   const uint32_t tmem = ctl.tmem_base;
   const Units units(a.T, a.H);
   if (bad && tid == 0) record_error(a.err, LA_ERR_DEVICE, KID_ATTN_TC, n_slots, -1);
@@ -315,17 +319,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (uint32_t i = (kc > kKSt ? kc - kKSt : 0); i < kc; ++i) {
         const uint32_t b = smem_u32(&ctl.k_full[i % kKSt]);
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(b, (i / kKSt) & 1) && globaltimer() - t0 < kTimeoutNs) {}
+        while (!mbar_try_wait(b, (i / kKSt) & 1) && globaltimer() - t0 < limit_ns) {}
       }
       for (uint32_t i = (vc > kVSt ? vc - kVSt : 0); i < vc; ++i) {
         const uint32_t b = smem_u32(&ctl.v_full[i % kVSt]);
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(b, (i / kVSt) & 1) && globaltimer() - t0 < kTimeoutNs) {}
+        while (!mbar_try_wait(b, (i / kVSt) & 1) && globaltimer() - t0 < limit_ns) {}
       }
       if (qc > 0) {
         const uint32_t b = smem_u32(&ctl.q_full);
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(b, (qc - 1) & 1) && globaltimer() - t0 < kTimeoutNs) {}
+        while (!mbar_try_wait(b, (qc - 1) & 1) && globaltimer() - t0 < limit_ns) {}
       }
     }
   } else if (warp == 1) {
@@ -335,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const uint32_t idesc_pv = F8 ? idesc_e4m3(kBM, kD, 0, 1) : idesc_bf16(kBM, kD, 0, 1);
       uint32_t kc = 0, vc = 0, qc = 0, pc0 = 0, pc1 = 0;
       bool ok = true;
+      if (a.stall) ok = wait(ctl.never, 0, 31);     // injected: runs out, latches a timeout
       // Shared-memory descriptors are built once; a tile or K-step offset is
       // added to the 14-bit start-address field (addresses >> 4, all below
       // 256 KB, so the add never carries out of the field).  Few
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       // every MMA issued has completed before TMEM is released
       tc_commit(smem_u32(&ctl.mma_done));
       const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(smem_u32(&ctl.mma_done), 0) && globaltimer() - t0 < kTimeoutNs) {}
+      while (!mbar_try_wait(smem_u32(&ctl.mma_done), 0) && globaltimer() - t0 < limit_ns) {}
     }
    }
   } else {

@@ -57,6 +57,7 @@ struct la_cache {
   CUtensorMap tm_q{}, tm_kv{}, tm_cur{}, tm_mem{};
   int num_sms = 148;
   std::vector<cudaEvent_t> prof_start, prof_stop;
+  int inject_stall = 0;             // tensor-core launches still to stall (tests)
   size_t prof_next = 0;
 };
 
@@ -840,6 +841,9 @@ la_status chunk_attention(la_cache* c, int layer, const void* q, const void* k_c
     ta.G = c->L.G;
     ta.mem_row0 = layer * 3 * g.num_heads;
     ta.scale_log2 = g.softmax_scale * 1.4426950408889634f;
+    ta.stall = c->inject_stall > 0;
+    if (ta.stall) --c->inject_stall;
+    ta.timeout_ns = ta.stall ? 100000000ull : 2000000000ull;   // 0.1 s injected, else 2 s
     ta.err = err;
     const bool prof = c->prof_next < c->prof_start.size();
     if (prof) cudaEventRecord(c->prof_start[c->prof_next], s);
@@ -1061,6 +1065,14 @@ la_status la_set_profile_events(la_cache_t* c, void* const* starts, void* const*
 }
 
 uint64_t la_launch_count(void) { return la::g_launches.load(std::memory_order_relaxed); }
+
+la_status la_debug_inject(la_cache_t* c, int what, int count) {
+  if (!c || count < 0) return LA_ERR_INVALID_ARG;
+  if (what != LA_INJECT_ATTN_STALL) return LA_ERR_INVALID_ARG;
+  if (!c->tc) return LA_ERR_UNSUPPORTED;
+  c->inject_stall = count;
+  return LA_OK;
+}
 
 la_status la_debug_memory(la_cache_t* c, int layer, void** k_raw, void** v, void** k_rot,
                           int* n_tokens, int* oldest) {

@@ -183,6 +183,9 @@ struct TcAttnArgs {
   const float* q_scales;      // e4m3: [H][T]
   int n_frames;               // frames per layer (bound of ctx->frame)
   int kv_f8;                  // 1: e4m3 K/V and queries, kind::f8f6f4
+  uint64_t timeout_ns;        // limit of every wait in the kernel
+  int stall;                  // failure injection: the MMA thread first waits on a
+                              // barrier nothing completes (runs into timeout_ns)
   void* out;           // [T][H][D] bf16
   int T, H;
   int layer_frame0;    // first frame page row of this layer in tm_kv, in pages

@@ -247,6 +247,17 @@ la_status la_debug_memory(la_cache_t* cache, int layer, void** k_raw, void** v, 
  * recording off.  The arrays are copied; the events stay the caller's. */
 la_status la_set_profile_events(la_cache_t* cache, void* const* starts, void* const* stops, int n);
 
+/* Failure injection for tests of the failure path (no GPU fault is made).
+ * LA_INJECT_ATTN_STALL: the next `count` tensor-core attention launches of
+ * this cache first wait on a barrier that nothing completes, with a 0.1 s
+ * limit.  The wait runs out, the kernel latches LA_ERR_TIMEOUT in the error
+ * word, drains its in-flight copies and MMAs, frees its tensor memory and
+ * returns; la_get_error then reports LA_ERR_TIMEOUT and the CUDA context
+ * stays usable.  LA_ERR_UNSUPPORTED when the cache runs the CUDA-core
+ * kernel. */
+#define LA_INJECT_ATTN_STALL 1
+la_status la_debug_inject(la_cache_t* cache, int what, int count);
+
 /* Number of kernels this library has enqueued since it was loaded. */
 uint64_t la_launch_count(void);
 

@@ -22,6 +22,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "la_internal.h"
 
 using namespace la;
@@ -67,6 +69,13 @@ void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order
 }  // namespace la
 
 namespace {
+
+// NVTX range around a public call (shows the library's phases on a
+// profiler timeline; costs nothing when no tool is attached).
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+};
 
 constexpr size_t kAlign = 1024;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -428,6 +437,7 @@ la_status la_context_plan(const la_cache_config* cfg, int block, const int32_t* 
 
 la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t pool_bytes,
                           const void* conv_w, void* stream, la_cache_t** out) {
+  Range nvtx_range("la_cache_create");
   if (!out) return LA_ERR_INVALID_ARG;
   *out = nullptr;
   la_status st = validate(cfg);
@@ -519,6 +529,7 @@ la_status la_cache_destroy(la_cache_t* c) {
 
 la_status la_select_context(la_cache_t* c, const float* query_pose, la_context* out,
                             void* stream) {
+  Range nvtx_range("la_select_context");
   la_status st = check_usable(c);
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
@@ -649,6 +660,7 @@ la_status la_select_context(la_cache_t* c, const float* query_pose, la_context* 
 
 la_status la_fill_block(la_cache_t* c, int layer, int block_id, const void* k, const void* v,
                         void* stream) {
+  Range nvtx_range("la_fill_block");
   la_status st = check_usable(c);
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
@@ -666,6 +678,7 @@ la_status la_fill_block(la_cache_t* c, int layer, int block_id, const void* k, c
 
 la_status la_prefetch_context(la_cache_t* c, const float* next_pose, la_context* out,
                               void* stream) {
+  Range nvtx_range("la_prefetch_context");
   la_status st = check_usable(c);
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
@@ -709,6 +722,7 @@ la_status la_prefetch_context(la_cache_t* c, const float* next_pose, la_context*
 
 la_status la_fill_window(la_cache_t* c, int layer, int block_id, const void* k, const void* v,
                          void* stream) {
+  Range nvtx_range("la_fill_window");
   la_status st = check_usable(c);
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
@@ -725,6 +739,7 @@ la_status la_fill_window(la_cache_t* c, int layer, int block_id, const void* k, 
 }
 
 la_status la_refresh_sink(la_cache_t* c, int layer, const void* k, const void* v, void* stream) {
+  Range nvtx_range("la_refresh_sink");
   la_status st = check_usable(c);
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
@@ -738,6 +753,7 @@ la_status la_refresh_sink(la_cache_t* c, int layer, const void* k, const void* v
 }
 
 la_status la_cache_load_history(la_cache_t* c, const float* kps, int n, void* stream) {
+  Range nvtx_range("la_cache_load_history");
   la_status st = check_usable(c);
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
@@ -887,11 +903,13 @@ extern "C" {
 
 la_status la_chunk_attention(la_cache_t* c, int layer, const void* q, const void* k_cur,
                              const void* v_cur, void* out, void* stream) {
+  Range nvtx_range("la_chunk_attention");
   return chunk_attention(c, layer, q, k_cur, v_cur, out, static_cast<cudaStream_t>(stream), false);
 }
 
 la_status la_cache_append_block(la_cache_t* c, int layer, const void* k, const void* v,
                                 void* stream) {
+  Range nvtx_range("la_cache_append_block");
   la_status st = check_usable(c);
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
@@ -976,6 +994,7 @@ la_status la_cache_append_block(la_cache_t* c, int layer, const void* k, const v
 la_status la_stream_step(la_cache_t* c, const float* pose, int n_steps, const void* const* q,
                          const void* const* k, const void* const* v, void* const* out,
                          la_fill_fn fill, void* user, void* stream) {
+  Range nvtx_range("la_stream_step");
   la_status st = check_usable(c);
   if (st != LA_OK) return st;
   const int L = c->cfg.num_layers;
@@ -1007,6 +1026,7 @@ la_status la_stream_step(la_cache_t* c, const float* pose, int n_steps, const vo
 }
 
 la_status la_get_error(la_cache_t* c, char* msg, size_t cap) {
+  Range nvtx_range("la_get_error");
   if (!c) return LA_ERR_INVALID_ARG;
   DevError e{};
   cudaError_t ce = cudaDeviceSynchronize();

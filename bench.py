@@ -205,7 +205,8 @@ class ClockSampler:
 def kernel_traffic(sc):
     """DRAM bytes (read + write) per attention launch from the committed ncu
     summary of this workload, or None when the summary is missing or was
-    taken on a different kernel source (its sha256 is recorded in it)."""
+    taken on different kernel code (the sha256 of the kernel file's device
+    code, up to its host launchers, is recorded in it)."""
     import hashlib
     import re
     name = {"c3_14b": "attn_tc_kernel_bf16_c3_14b.md", "c5_fp8": "attn_tc_kernel_e4m3_c5_fp8.md"}
@@ -213,8 +214,9 @@ def kernel_traffic(sc):
     if not os.path.isfile(path):
         return None
     text = open(path).read()
-    src = os.path.join(ROOT, "bounded_kv_cache_la_b300", "csrc", "k_attn_tc.cu")
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    # the kernel = the file's device code, everything before its host launchers
+    src = open(os.path.join(ROOT, "bounded_kv_cache_la_b300", "csrc", "k_attn_tc.cu")).read()
+    digest = hashlib.sha256(src[:src.index("bool attn_tc_supported")].encode()).hexdigest()
     m_src = re.search(r"kernel source sha256: ([0-9a-f]{64})", text)
     m_tr = re.search(r"traffic_bytes_per_launch: (\d+)", text)
     if not m_src or not m_tr or m_src.group(1) != digest:

@@ -636,12 +636,17 @@ bool attn_tc_supported(int D, int kv_dtype) {
 
 template <bool F8>
 static cudaError_t launch_attn_tc_t(const TcAttnArgs& a, int num_sms, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Tile<F8>::kSmem);
+  // the shared-memory opt-in is a per-device function attribute
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(attn_tc_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tile<F8>::kSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   const int n_pairs = (a.T + 2 * kBM - 1) / (2 * kBM);
   const int units = a.H * n_pairs;

@@ -120,8 +120,8 @@ size_t la_cache_required_bytes(const la_cache_config* cfg);
 la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t pool_bytes,
                           const void* conv_w, void* stream, la_cache_t** out);
 
-/* Releases the host state.  Synchronises `stream`-less: call it only after
- * the work of the cache has completed.  The pool stays the caller's. */
+/* Releases the host state.  It does not synchronise: call it only after the
+ * work enqueued for this cache has completed.  The pool stays the caller's. */
 la_status la_cache_destroy(la_cache_t* cache);
 
 /* Starts block b (b = number of blocks appended so far).  Runs the pose
@@ -166,7 +166,10 @@ la_status la_prefetch_context(la_cache_t* cache, const float* next_pose, la_cont
  * at temporal base t0 holds positions (t0 + frame, row, column).
  * q, k_cur, v_cur: device [T][H][D] q_dtype (the current block's values at
  * this denoising step); out: device [T][H][D] q_dtype.
- * out = softmax(softmax_scale * RoPE(q) RoPE(K_ctx)^T) V_ctx, per head. */
+ * out = softmax(softmax_scale * RoPE(q) RoPE(K_ctx)^T) V_ctx, per head.
+ * With an e4m3 cache the tensor-core kernel also rounds the rotated queries
+ * (one scale per head and token) and the probabilities to e4m3 ([LX]
+ * 技术内核: FP8 attention). */
 la_status la_chunk_attention(la_cache_t* cache, int layer, const void* q, const void* k_cur,
                              const void* v_cur, void* out, void* stream);
 
@@ -201,7 +204,10 @@ typedef la_status (*la_fill_fn)(la_cache_t* cache, int layer, int block_id, void
 /* One streamed block: select, n_steps x L chunk attentions, then L appends
  * of the last step's K/V.  q, k, v, out: host arrays of n_steps*L device
  * pointers, entry [step * L + layer].  `fill` (required in EXTERNAL mode
- * when a fill is needed) is called between select and the attentions. */
+ * when a fill is needed) is called between select and the attentions.  The
+ * last step's attention writes the block's K/V pages straight into the
+ * block's own cache frame, so the appends that follow copy nothing (for
+ * ConvKV they still compress the block leaving the window). */
 la_status la_stream_step(la_cache_t* cache, const float* pose, int n_steps,
                          const void* const* q, const void* const* k, const void* const* v,
                          void* const* out, la_fill_fn fill, void* user, void* stream);

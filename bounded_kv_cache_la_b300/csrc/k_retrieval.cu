@@ -32,6 +32,26 @@ __device__ __forceinline__ unsigned long long make_key(float s, int id) {
   return ((unsigned long long)orderable(s) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
 }
 
+// Pose descriptor of 17 (x, y) keypoints, one warp: lane l < 17 gets its
+// keypoint centred by the per-axis mean, every lane the inverse norm of the
+// 34-vector (0 for a zero vector).  Shared by the retrieval and the batch
+// history load so that both write bit-identical table rows.
+__device__ __forceinline__ void pose_descriptor(float x, float y, int lane, float& cx, float& cy,
+                                                float& inv) {
+  if (lane >= 17) { x = 0.f; y = 0.f; }
+  float sx = x, sy = y;
+  for (int o = 16; o; o >>= 1) {
+    sx += __shfl_xor_sync(0xffffffffu, sx, o);
+    sy += __shfl_xor_sync(0xffffffffu, sy, o);
+  }
+  cx = x - sx / 17.f;
+  cy = y - sy / 17.f;
+  if (lane >= 17) { cx = 0.f; cy = 0.f; }
+  float ss = cx * cx + cy * cy;
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  inv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+}
+
 __global__ void __launch_bounds__(kThreads) retrieval_kernel(RetrievalArgs a) {
   __shared__ __align__(16) float q[36];
   __shared__ float inv_q;
@@ -43,18 +63,11 @@ __global__ void __launch_bounds__(kThreads) retrieval_kernel(RetrievalArgs a) {
   if (warp == 0) {
     float x = 0.f, y = 0.f;
     if (lane < 17) { x = a.kp[2 * lane]; y = a.kp[2 * lane + 1]; }
-    float sx = x, sy = y;
-    for (int o = 16; o; o >>= 1) {
-      sx += __shfl_xor_sync(0xffffffffu, sx, o);
-      sy += __shfl_xor_sync(0xffffffffu, sy, o);
-    }
-    float cx = x - sx / 17.f, cy = y - sy / 17.f;
-    if (lane >= 17) { cx = 0.f; cy = 0.f; }
-    float ss = cx * cx + cy * cy;
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    float cx, cy, inv;
+    pose_descriptor(x, y, lane, cx, cy, inv);
     if (lane < 17) { q[2 * lane] = cx; q[2 * lane + 1] = cy; }
     if (lane < 2) q[34 + lane] = 0.f;
-    if (lane == 0) inv_q = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+    if (lane == 0) inv_q = inv;
   }
   __syncthreads();
 
@@ -146,7 +159,30 @@ __global__ void __launch_bounds__(kThreads) retrieval_kernel(RetrievalArgs a) {
   }
 }
 
+// Batch history load: row i of `table` holds block i's raw keypoints in its
+// first 34 floats; one warp per row turns them into the descriptor row (as
+// the retrieval kernel writes it) and the inverse norm.
+__global__ void __launch_bounds__(256) pose_rows_kernel(float* table, float* inv_norm, int n) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= n) return;                      // whole warps leave together
+  float* r = table + (size_t)row * 36;
+  float x = 0.f, y = 0.f;
+  if (lane < 17) { x = r[2 * lane]; y = r[2 * lane + 1]; }
+  float cx, cy, inv;
+  pose_descriptor(x, y, lane, cx, cy, inv);  // every lane has read before any writes
+  if (lane < 17) { r[2 * lane] = cx; r[2 * lane + 1] = cy; }
+  if (lane < 2) r[34 + lane] = 0.f;
+  if (lane == 0) inv_norm[row] = inv;
+}
+
 }  // namespace
+
+cudaError_t launch_pose_rows(float* table, float* inv_norm, int n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  pose_rows_kernel<<<(n + 7) / 8, 256, 0, s>>>(table, inv_norm, n);
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_retrieval(const RetrievalArgs& a, cudaStream_t s) {
   int n = a.c1 > a.c0 ? a.c1 - a.c0 : 0;

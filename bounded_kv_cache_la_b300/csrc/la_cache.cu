@@ -761,21 +761,18 @@ la_status la_cache_load_history(la_cache_t* c, const float* kps, int n, void* st
   if (c->b != 0 || c->selected) return LA_ERR_STATE;
   if (!kps || n < 1 || n >= g.max_history) return LA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  for (int i = 0; i < n; ++i) {
-    RetrievalArgs a{};
-    std::memcpy(a.kp, kps + (size_t)i * 34, sizeof(a.kp));
-    a.pose_row = i;
-    a.c0 = a.c1 = 0;
-    a.k = 0;
-    a.max_history = g.max_history;
-    a.table = reinterpret_cast<float*>(c->pool + c->L.pose_tab);
-    a.inv_norm = reinterpret_cast<float*>(c->pool + c->L.inv_norm);
-    a.scores = reinterpret_cast<float*>(c->pool + c->L.scores);
-    a.topk = reinterpret_cast<DevTopk*>(c->pool + c->L.topk);
-    a.err = reinterpret_cast<DevError*>(c->pool + c->L.err);
-    st = cuda_status(c, launch_retrieval(a, s), "pose history");
-    if (st != LA_OK) return st;
-  }
+  for (size_t i = 0; i < (size_t)n * 34; ++i)
+    if (!std::isfinite(kps[i])) return LA_ERR_INVALID_ARG;
+  // raw keypoints into the first 34 floats of each table row, then one
+  // kernel turns every row into its descriptor
+  float* table = reinterpret_cast<float*>(c->pool + c->L.pose_tab);
+  st = cuda_status(c, cudaMemcpy2DAsync(table, 36 * sizeof(float), kps, 34 * sizeof(float),
+                                        34 * sizeof(float), n, cudaMemcpyHostToDevice, s),
+                   "upload pose history");
+  if (st == LA_OK)
+    st = cuda_status(c, launch_pose_rows(table, reinterpret_cast<float*>(c->pool + c->L.inv_norm), n, s),
+                     "pose history");
+  if (st != LA_OK) return st;
   c->b = n;
   std::vector<int> need = window_blocks(g, n);
   if (g.static_sink) need.insert(need.begin(), 0);

@@ -106,6 +106,9 @@ struct RetrievalArgs {
   DevError* err;
 };
 cudaError_t launch_retrieval(const RetrievalArgs& a, cudaStream_t s);
+// Rows 0..n-1 of `table` hold raw keypoints (34 floats each): turned into
+// descriptor rows and inverse norms in place.
+cudaError_t launch_pose_rows(float* table, float* inv_norm, int n, cudaStream_t s);
 
 struct AppendArgs {
   const void* k;       // [T][H][D] src_dtype

@@ -4,6 +4,7 @@ ConvKV memory, attention outputs within the stated tolerances)."""
 import numpy as np
 import pytest
 
+from bounded_kv_cache_la_b300 import capi
 from oracle import e4m3, rope, stream as ostream
 from synth import C1_TINY, C2_MID, C3_14B, C4_CONVKV, C5_FP8, gen
 
@@ -206,3 +207,29 @@ def test_call_order_errors():
     with pytest.raises(capi.LaError) as e:
         cache.la_select_context(bad)
     assert e.value.status == capi.LA_ERR_INVALID_ARG
+
+
+def test_history_load_rows_equal_retrieval_rows():
+    """la_cache_load_history writes every pose row in one launch; the rows
+    must be bit-identical to those the retrieval kernel writes block by
+    block (here through la_pose_topk_noalloc), so the scores agree exactly."""
+    import torch
+    sc = C5_FP8.with_(grid_h=4, grid_w=4, num_heads=2)
+    n = 700
+    kps = gen.poses(sc, n_blocks=n + 1)
+    cache = H.make_cache(sc.with_(num_layers=1), max_history=n + 8)
+    cache.la_cache_load_history(kps[:n].reshape(n, 34))
+    ctx = cache.la_select_context(kps[n])
+    table = torch.zeros((n + 1, 36), dtype=torch.float32, device="cuda")
+    inv = torch.zeros(n + 1, dtype=torch.float32, device="cuda")
+    k = sc.dyn_topk
+    ids = torch.empty(k + 1, dtype=torch.int32, device="cuda")
+    scores = torch.empty(k + 1, dtype=torch.float32, device="cuda")
+    n_out = torch.empty(1, dtype=torch.int32, device="cuda")
+    for b in range(n):
+        capi.la_pose_topk_noalloc(table, inv, kps[b], b, 0, 0, 0, ids, scores, n_out)
+    capi.la_pose_topk_noalloc(table, inv, kps[n], n, 1, n - sc.window, k, ids, scores, n_out)
+    torch.cuda.synchronize()
+    got = sorted(zip(ids.cpu().numpy()[:k].tolist(), scores.cpu().numpy()[:k].tolist()))
+    assert [g[0] for g in got] == ctx["dyn_ids"]
+    assert [np.float32(g[1]) for g in got] == [np.float32(x) for x in ctx["dyn_scores"]]

@@ -48,8 +48,11 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   return *reinterpret_cast<uint16_t*>(&h);
 }
 
+// Two fp32 -> bf16 (round to nearest even) in one instruction; lo in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 
 // e4m3 with round-to-nearest-even and saturation to +-448 (cvt.rn.satfinite).
@@ -63,12 +66,15 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
   return __half2float(*reinterpret_cast<__half*>(&h));
 }
 
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  return (__umulhi(n, f.m) + n) >> f.l;
+}
+
 // Token index (raster order) -> (frame, row, column).
 __device__ __forceinline__ void token_pos(const RopeDims& r, int t, int& f, int& h, int& w) {
-  int hw = r.GH * r.GW;
-  f = t / hw;
-  int rem = t - f * hw;
-  h = rem / r.GW;
+  f = (int)fdiv((uint32_t)t, r.div_hw);
+  const int rem = t - f * (int)r.div_hw.d;
+  h = (int)fdiv((uint32_t)rem, r.div_w);
   w = rem - h * r.GW;
 }
 

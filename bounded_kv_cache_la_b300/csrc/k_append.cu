@@ -7,7 +7,8 @@
 // (head, block) with scale = amax / 448, in two passes (amax, then codes).
 //
 // One thread moves 16 source bytes (8 bf16 or 4 fp32 values) of one
-// (token, head); consecutive threads read consecutive 16-byte chunks.
+// (token, head); a CTA covers consecutive tokens of one head, and
+// consecutive threads read consecutive 16-byte chunks of a token's row.
 #include "dev_common.cuh"
 
 namespace la {
@@ -18,8 +19,7 @@ template <int SRC>  // LA_F32 or LA_BF16
 struct Src;
 template <> struct Src<LA_BF16> {
   static constexpr int kVec = 8;
-  __device__ static void load(const void* base, size_t off, float* x) {
-    uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(base) + off);
+  __device__ static void unpack(const uint4& u, float* x) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -27,12 +27,18 @@ template <> struct Src<LA_BF16> {
       x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
   }
+  __device__ static void load(const void* base, size_t off, float* x) {
+    unpack(*reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(base) + off), x);
+  }
 };
 template <> struct Src<LA_F32> {
   static constexpr int kVec = 4;
+  __device__ static void unpack(const uint4& u, float* x) {
+    x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+    x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
+  }
   __device__ static void load(const void* base, size_t off, float* x) {
-    float4 u = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + off);
-    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    unpack(*reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(base) + off), x);
   }
 };
 
@@ -71,59 +77,82 @@ __device__ __forceinline__ void rotate_chunk(const RopeDims& r, int t, int d0, f
   }
 }
 
+// Grid: x = token tile (256 / chunks tokens), y = head; one thread per
+// chunk of VEC dims.  Reads of a token's head row and writes of the page
+// rows stay 16-byte vectors; index math is 32-bit, once per thread.
+struct Item {
+  int t, h, c;
+  bool live;
+};
+__device__ __forceinline__ Item page_item(const AppendArgs& a, int chunks) {
+  const int per_cta = blockDim.x / chunks;
+  Item it;
+  it.h = blockIdx.y;
+  it.t = blockIdx.x * per_cta + (int)threadIdx.x / chunks;
+  it.c = (int)threadIdx.x % chunks;
+  it.live = it.t < a.T;
+  return it;
+}
+
+// Values and the raw-key copy keep their dtype, so they move as raw 16-byte
+// words; only the key is unpacked, turned and repacked.
 template <int SRC>
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   constexpr int VEC = Src<SRC>::kVec;
-  const int chunks = a.D / VEC;
-  const long long total = (long long)a.T * a.H * chunks;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    int c = (int)(i % chunks);
-    long long th = i / chunks;
-    int h = (int)(th % a.H);
-    int t = (int)(th / a.H);
-    size_t src_off = (size_t)th * a.D + c * VEC;                      // [t][h][d]
-    size_t dst_off = ((size_t)h * a.T + t) * a.D + c * VEC;           // [h][t][d]
-    float k[VEC], v[VEC];
-    Src<SRC>::load(a.k, src_off, k);
-    Src<SRC>::load(a.v, src_off, v);
+  constexpr int ELT = SRC == LA_BF16 ? 2 : 4;
+  const Item it = page_item(a, a.D / VEC);
+  if (!it.live) return;
+  const size_t src_off = ((size_t)it.t * a.H + it.h) * a.D + it.c * VEC;     // [t][h][d]
+  const size_t dst_off = ((size_t)it.h * a.T + it.t) * a.D + it.c * VEC;     // [h][t][d]
+  const uint4 kw = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(a.k) + src_off * ELT);
+  const uint4 vw = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(a.v) + src_off * ELT);
+  float k[VEC];
+  Src<SRC>::unpack(kw, k);
+  if (a.dst_dtype == SRC) {
+    if (a.kraw_dst) *reinterpret_cast<uint4*>(reinterpret_cast<char*>(a.kraw_dst) + dst_off * ELT) = kw;
+    *reinterpret_cast<uint4*>(reinterpret_cast<char*>(a.v_dst) + dst_off * ELT) = vw;
+  } else {
+    float v[VEC];
+    Src<SRC>::unpack(vw, v);
     if (a.kraw_dst) store_vec<VEC>(a.kraw_dst, dst_off, a.dst_dtype, k);
-    rotate_chunk<VEC>(a.rope, t, c * VEC, k);
-    store_vec<VEC>(a.k_dst, dst_off, a.dst_dtype, k);
     store_vec<VEC>(a.v_dst, dst_off, a.dst_dtype, v);
   }
+  rotate_chunk<VEC>(a.rope, it.t, it.c * VEC, k);
+  store_vec<VEC>(a.k_dst, dst_off, a.dst_dtype, k);
 }
 
-// e4m3 pass 1: per-head amax of the rotated keys and of the values.
+// e4m3 pass 1: per-head amax of the rotated keys and of the values (one
+// head per CTA: a warp max, then one shared and one global atomic per warp).
 template <int SRC>
 __global__ void __launch_bounds__(256) amax_kernel(AppendArgs a) {
   constexpr int VEC = Src<SRC>::kVec;
-  __shared__ unsigned int sm[2][64];
-  for (int i = threadIdx.x; i < 128; i += blockDim.x) (&sm[0][0])[i] = 0u;
-  __syncthreads();
-  const int chunks = a.D / VEC;
-  const long long total = (long long)a.T * a.H * chunks;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    int c = (int)(i % chunks);
-    long long th = i / chunks;
-    int h = (int)(th % a.H);
-    int t = (int)(th / a.H);
-    size_t src_off = (size_t)th * a.D + c * VEC;
+  const Item it = page_item(a, a.D / VEC);
+  float mk = 0.f, mv = 0.f;
+  if (it.live) {
+    const size_t src_off = ((size_t)it.t * a.H + it.h) * a.D + it.c * VEC;
     float k[VEC], v[VEC];
     Src<SRC>::load(a.k, src_off, k);
     Src<SRC>::load(a.v, src_off, v);
-    rotate_chunk<VEC>(a.rope, t, c * VEC, k);
-    float mk = 0.f, mv = 0.f;
+    rotate_chunk<VEC>(a.rope, it.t, it.c * VEC, k);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) { mk = fmaxf(mk, fabsf(k[j])); mv = fmaxf(mv, fabsf(v[j])); }
-    atomicMax(&sm[0][h], __float_as_uint(mk));
-    atomicMax(&sm[1][h], __float_as_uint(mv));
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+    mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+  }
+  __shared__ unsigned int sm[2];
+  if (threadIdx.x < 2) sm[threadIdx.x] = 0u;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    atomicMax(&sm[0], __float_as_uint(mk));
+    atomicMax(&sm[1], __float_as_uint(mv));
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < a.H; i += blockDim.x) {
-    if (sm[0][i]) atomicMax(&a.amax[i], sm[0][i]);
-    if (sm[1][i]) atomicMax(&a.amax[a.H + i], sm[1][i]);
+  if (threadIdx.x == 0) {
+    if (sm[0]) atomicMax(&a.amax[it.h], sm[0]);
+    if (sm[1]) atomicMax(&a.amax[a.H + it.h], sm[1]);
   }
 }
 
@@ -131,65 +160,54 @@ __global__ void __launch_bounds__(256) amax_kernel(AppendArgs a) {
 template <int SRC>
 __global__ void __launch_bounds__(256) quant_kernel(AppendArgs a) {
   constexpr int VEC = Src<SRC>::kVec;
-  const int chunks = a.D / VEC;
-  const long long total = (long long)a.T * a.H * chunks;
-  if (blockIdx.x == 0) {
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
     for (int i = threadIdx.x; i < 2 * a.H; i += blockDim.x) {
       float am = __uint_as_float(a.amax[i]);
       float sc = am > 0.f ? __fdiv_rn(am, 448.f) : 1.f;
       if (i < a.H) a.k_scale[i] = sc; else a.v_scale[i - a.H] = sc;
     }
   }
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    int c = (int)(i % chunks);
-    long long th = i / chunks;
-    int h = (int)(th % a.H);
-    int t = (int)(th / a.H);
-    size_t src_off = (size_t)th * a.D + c * VEC;
-    size_t dst_off = ((size_t)h * a.T + t) * a.D + c * VEC;
-    float k[VEC], v[VEC];
-    Src<SRC>::load(a.k, src_off, k);
-    Src<SRC>::load(a.v, src_off, v);
-    rotate_chunk<VEC>(a.rope, t, c * VEC, k);
-    float amk = __uint_as_float(a.amax[h]), amv = __uint_as_float(a.amax[a.H + h]);
-    float ik = amk > 0.f ? __fdiv_rn(448.f, amk) : 0.f;
-    float iv = amv > 0.f ? __fdiv_rn(448.f, amv) : 0.f;
-    uint8_t ck[VEC], cv[VEC];
+  const Item it = page_item(a, a.D / VEC);
+  if (!it.live) return;
+  const int h = it.h;
+  const size_t src_off = ((size_t)it.t * a.H + h) * a.D + it.c * VEC;
+  const size_t dst_off = ((size_t)h * a.T + it.t) * a.D + it.c * VEC;
+  float k[VEC], v[VEC];
+  Src<SRC>::load(a.k, src_off, k);
+  Src<SRC>::load(a.v, src_off, v);
+  rotate_chunk<VEC>(a.rope, it.t, it.c * VEC, k);
+  float amk = __uint_as_float(a.amax[h]), amv = __uint_as_float(a.amax[a.H + h]);
+  float ik = amk > 0.f ? __fdiv_rn(448.f, amk) : 0.f;
+  float iv = amv > 0.f ? __fdiv_rn(448.f, amv) : 0.f;
+  uint8_t ck[VEC], cv[VEC];
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-      ck[j] = f32_to_e4m3(__fmul_rn(k[j], ik));
-      cv[j] = f32_to_e4m3(__fmul_rn(v[j], iv));
-    }
-    uint8_t* pk = reinterpret_cast<uint8_t*>(a.k_dst) + dst_off;
-    uint8_t* pv = reinterpret_cast<uint8_t*>(a.v_dst) + dst_off;
-    if (VEC == 8) {
-      uint2 uk, uv;
-      uk.x = ck[0] | (ck[1] << 8) | (ck[2] << 16) | ((uint32_t)ck[3] << 24);
-      uk.y = ck[4] | (ck[5] << 8) | (ck[6] << 16) | ((uint32_t)ck[7] << 24);
-      uv.x = cv[0] | (cv[1] << 8) | (cv[2] << 16) | ((uint32_t)cv[3] << 24);
-      uv.y = cv[4] | (cv[5] << 8) | (cv[6] << 16) | ((uint32_t)cv[7] << 24);
-      *reinterpret_cast<uint2*>(pk) = uk;
-      *reinterpret_cast<uint2*>(pv) = uv;
-    } else {
-      *reinterpret_cast<uint32_t*>(pk) = ck[0] | (ck[1] << 8) | (ck[2] << 16) | ((uint32_t)ck[3] << 24);
-      *reinterpret_cast<uint32_t*>(pv) = cv[0] | (cv[1] << 8) | (cv[2] << 16) | ((uint32_t)cv[3] << 24);
-    }
+  for (int j = 0; j < VEC; ++j) {
+    ck[j] = f32_to_e4m3(__fmul_rn(k[j], ik));
+    cv[j] = f32_to_e4m3(__fmul_rn(v[j], iv));
   }
-}
-
-int grid_for(long long work) {
-  long long g = (work + 255) / 256;
-  if (g > 148LL * 16) g = 148LL * 16;
-  return (int)(g < 1 ? 1 : g);
+  uint8_t* pk = reinterpret_cast<uint8_t*>(a.k_dst) + dst_off;
+  uint8_t* pv = reinterpret_cast<uint8_t*>(a.v_dst) + dst_off;
+  if (VEC == 8) {
+    uint2 uk, uv;
+    uk.x = ck[0] | (ck[1] << 8) | (ck[2] << 16) | ((uint32_t)ck[3] << 24);
+    uk.y = ck[4] | (ck[5] << 8) | (ck[6] << 16) | ((uint32_t)ck[7] << 24);
+    uv.x = cv[0] | (cv[1] << 8) | (cv[2] << 16) | ((uint32_t)cv[3] << 24);
+    uv.y = cv[4] | (cv[5] << 8) | (cv[6] << 16) | ((uint32_t)cv[7] << 24);
+    *reinterpret_cast<uint2*>(pk) = uk;
+    *reinterpret_cast<uint2*>(pv) = uv;
+  } else {
+    *reinterpret_cast<uint32_t*>(pk) = ck[0] | (ck[1] << 8) | (ck[2] << 16) | ((uint32_t)ck[3] << 24);
+    *reinterpret_cast<uint32_t*>(pv) = cv[0] | (cv[1] << 8) | (cv[2] << 16) | ((uint32_t)cv[3] << 24);
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
   const int vec = a.src_dtype == LA_BF16 ? 8 : 4;
-  long long work = (long long)a.T * a.H * (a.D / vec);
-  int grid = grid_for(work);
+  const int chunks = a.D / vec;                       // 8, 16 or 32: divides 256
+  if (a.D % vec || 256 % chunks || a.H < 1 || a.H > 65535 || a.T < 1) return cudaErrorInvalidValue;
+  const dim3 grid((a.T + 256 / chunks - 1) / (256 / chunks), a.H);
   if (a.dst_dtype == LA_E4M3) {
     cudaError_t e = cudaMemsetAsync(a.amax, 0, sizeof(unsigned int) * 2 * a.H, s);
     if (e != cudaSuccess) return e;

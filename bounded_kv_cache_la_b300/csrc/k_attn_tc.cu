@@ -300,9 +300,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
               if (!(ok = wait(ctl.q_empty, (qc & 1) ^ 1, 2))) break;
               mbar_arrive_expect_tx(smem_u32(&ctl.q_full), n_qt * Tl::kBytes);
               for (int qi = 0; qi < n_qt; ++qi)
-                for (int bx = 0; bx < Tl::kBoxes; ++bx)
-                  tma_load_3d(sQ + qi * Tl::kBytes + bx * Tl::kBoxBytes, &a.tm_q, bx * Tl::kBoxElems,
-                              row0 + qi * kBM, s * a.H + h, smem_u32(&ctl.q_full));
+                for (int bx = 0; bx < Tl::kBoxes; ++bx) {
+                  // split rows: box 1 is the slot-independent half, one copy per head
+                  const bool sh = a.q_shared_z >= 0 && bx == 1;
+                  tma_load_3d(sQ + qi * Tl::kBytes + bx * Tl::kBoxBytes, &a.tm_q,
+                              a.q_shared_z >= 0 ? 0 : bx * Tl::kBoxElems, row0 + qi * kBM,
+                              sh ? a.q_shared_z + h : s * a.H + h, smem_u32(&ctl.q_full));
+                }
               ++qc;
             }
             const int vs = vc % kVSt;
@@ -657,6 +661,7 @@ static cudaError_t launch_attn_tc_t(const TcAttnArgs& a, int num_sms, cudaStream
 }
 
 cudaError_t launch_attn_tc(const TcAttnArgs& a, int num_sms, cudaStream_t s) {
+  if (a.kv_f8 && a.q_shared_z >= 0) return cudaErrorInvalidValue;   // split rows are bf16 only
   return a.kv_f8 ? launch_attn_tc_t<true>(a, num_sms, s) : launch_attn_tc_t<false>(a, num_sms, s);
 }
 

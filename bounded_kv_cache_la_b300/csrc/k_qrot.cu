@@ -19,118 +19,150 @@ using namespace ptx;
 // bf16 cache: bf16 copies.  e4m3 cache: e4m3 codes with one fp32 scale per
 // (head, token), qscale[h][t] = m / 448 where m is the largest norm of the
 // token's 64 rotation pairs -- rotations keep pair norms, so one scale
-// serves every slot and no code saturates.  One thread per 8 dims; the 16
-// threads of a (token, head) are 16 consecutive lanes.
-template <bool F8>
+// serves every slot and no code saturates.
+// SPLIT (bf16, every temporal dim below D/2): the copies hold only the first
+// half of each row; the second half, the same for every slot, is written
+// once at slot index n_qrot.
+//
+// Grid: x = tile of 16 tokens, y = head; one thread per 8 dims.  Full rows:
+// the 16 threads of a token are 16 consecutive lanes.  SPLIT: warps 0-3 take
+// the first halves (8 lanes per token, one store per slot), warps 4-7 the
+// second halves (one store).  Index math is 32-bit and done once per thread;
+// the slot loop only steps the destination and picks the table row.
+constexpr int kTokensPerCta = 16;
+
+template <bool F8, bool SPLIT>
 __global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
+  __shared__ int s_dq[kMaxAttnSlots];                 // t0_cur - t0_s
+  __shared__ int s_bad;
   const DevContext& ctx = *a.ctx;
   const int n_slots = ctx.n_slots;
-  if (n_slots < 1 || n_slots > a.n_qrot) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) record_error(a.err, LA_ERR_DEVICE, KID_QROT, n_slots, a.n_qrot);
+  if (n_slots < 1 || n_slots > a.n_qrot || n_slots > kMaxAttnSlots) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+      record_error(a.err, LA_ERR_DEVICE, KID_QROT, n_slots, a.n_qrot);
     return;
   }
   // every slot's temporal offset must stay inside the RoPE table for every
   // frame of the block (checked up front so that all threads leave together)
-  for (int s = 0; s < n_slots; ++s) {
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  if ((int)threadIdx.x < n_slots) {
+    const int s = threadIdx.x;
     const int lo = ctx.t0_cur - ctx.t0[s], hi = lo + a.rope.F - 1;
+    s_dq[s] = lo;
     if (lo < 0 || hi >= a.rope.max_t) {
-      if (blockIdx.x == 0 && threadIdx.x == 0) record_error(a.err, LA_ERR_DEVICE, KID_QROT, lo, s);
-      return;
+      s_bad = 1;
+      if (blockIdx.x == 0 && blockIdx.y == 0) record_error(a.err, LA_ERR_DEVICE, KID_QROT, lo, s);
     }
   }
-  const int chunks = a.D / 8;
-  const long long total = (long long)a.T * a.H * chunks;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  // warp-uniform trip count (the e4m3 path reduces over 16-lane groups)
-  for (long long base = blockIdx.x * (long long)blockDim.x + (threadIdx.x & ~31); base < total;
-       base += stride) {
-    const long long idx = base + (threadIdx.x & 31);
-    const bool valid = idx < total;
-    const long long vi = valid ? idx : 0;
-    // consecutive threads: dims, then tokens of one head, so each slot copy
-    // ([slot][head][token][dim]) is written in long contiguous runs
-    const int cch = (int)(vi % chunks);
-    const long long ht = vi / chunks;
-    const int t = (int)(ht % a.T);
-    const int h = (int)(ht / a.T);
-    const size_t th = (size_t)t * a.H + h;
-    uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + th * a.D + cch * 8);
-    float x[8];
+  __syncthreads();
+  if (s_bad) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  int t, cch;
+  if (SPLIT) {
+    t = blockIdx.x * kTokensPerCta + (warp & 3) * 4 + (lane >> 3);
+    cch = (warp >= 4 ? 8 : 0) + (lane & 7);
+  } else {
+    t = blockIdx.x * kTokensPerCta + (threadIdx.x >> 4);
+    cch = threadIdx.x & 15;
+  }
+  const bool valid = t < a.T;
+  float x[8];
+  {
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) +
+                                                   ((size_t)t * a.H + h) * a.D + cch * 8);
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       x[2 * e] = __uint_as_float(w[e] << 16);
       x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
     }
-    float inv = 1.f;
-    if (F8) {
-      float n2 = 0.f;
+  }
+  float inv = 1.f;
+  if (F8) {                                           // all 32 lanes take part
+    float n2 = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) n2 = fmaxf(n2, x[2 * e] * x[2 * e] + x[2 * e + 1] * x[2 * e + 1]);
+    for (int e = 0; e < 4; ++e) n2 = fmaxf(n2, x[2 * e] * x[2 * e] + x[2 * e + 1] * x[2 * e + 1]);
 #pragma unroll
-      for (int o = 8; o; o >>= 1) n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
-      const float mn = sqrtf(n2);
-      inv = mn > 0.f ? 448.f / mn : 0.f;
-      if (valid && cch == 0) a.qscale[(size_t)h * a.T + t] = mn > 0.f ? mn / 448.f : 1.f;
+    for (int o = 8; o; o >>= 1) n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
+    const float mn = sqrtf(n2);
+    inv = mn > 0.f ? 448.f / mn : 0.f;
+    if (valid && cch == 0) a.qscale[(size_t)h * a.T + t] = mn > 0.f ? mn / 448.f : 1.f;
+  }
+  if (!valid) return;
+  int f, hh, ww;
+  token_pos(a.rope, t, f, hh, ww);
+  // Pairs in the height / width parts turn the same way for every slot:
+  // rotate them once.  Only temporal pairs (dims < dt) depend on the slot.
+  const int d0 = cch * 8;
+  float y[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    y[2 * e] = x[2 * e];
+    y[2 * e + 1] = x[2 * e + 1];
+    if (d0 + 2 * e >= a.rope.dt) {
+      const float2 r = rot_exact(x[2 * e], x[2 * e + 1], rope_cs(a.rope, d0 + 2 * e, 0, hh, ww));
+      y[2 * e] = r.x;
+      y[2 * e + 1] = r.y;
     }
-    if (!valid) continue;
-    int f, hh, ww;
-    token_pos(a.rope, t, f, hh, ww);
-    // Pairs in the height / width parts turn the same way for every slot:
-    // rotate them once.  Only temporal pairs (dims < dt) depend on the slot.
-    const int d0 = cch * 8;
-    float y[8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (d0 + 2 * e >= a.rope.dt) {
-        const float2 r = rot_exact(x[2 * e], x[2 * e + 1], rope_cs(a.rope, d0 + 2 * e, 0, hh, ww));
-        y[2 * e] = r.x;
-        y[2 * e + 1] = r.y;
-      }
-    }
-    const bool temporal = d0 < a.rope.dt;
-    uint4 fixed_bf16{};
-    uint2 fixed_f8{};
-    if (!temporal) {
-      if (F8) {
-        fixed_f8.x = cvt_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
-        fixed_f8.y = cvt_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv);
+  }
+  const int half = a.D / 2;
+  const int row_len = SPLIT ? half : a.D;
+  if (SPLIT && cch * 8 >= half) {                     // the shared second half
+    const size_t off = (((size_t)a.n_qrot * a.H + h) * a.T + t) * row_len + (d0 - half);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.qrot) + off) =
+        make_uint4(cvt_bf16x2(y[0], y[1]), cvt_bf16x2(y[2], y[3]), cvt_bf16x2(y[4], y[5]),
+                   cvt_bf16x2(y[6], y[7]));
+    return;
+  }
+  const size_t slot_stride = (size_t)a.H * a.T * row_len;
+  size_t off = ((size_t)h * a.T + t) * row_len + d0;
+  const int pair0 = d0 >> 1, pairs_t = a.rope.dt >> 1;
+  // temporal pairs of this chunk: 0..4; with dt a multiple of 4 they come in
+  // twos and a table row's pairs sit 16-byte aligned, so (cos, sin) of two
+  // pairs is one 16-byte load
+  const int np = min(max((a.rope.dt - d0) >> 1, 0), 4);
+  const bool vec = (a.rope.dt & 3) == 0;
+#pragma unroll 2
+  for (int s = 0; s < n_slots; ++s, off += slot_stride) {
+    if (np > 0) {
+      const float2* row = a.rope.tab_t + (size_t)(s_dq[s] + f) * pairs_t + pair0;
+      float2 cs[4];
+      if (vec) {
+        const float4 c01 = reinterpret_cast<const float4*>(row)[0];
+        cs[0] = make_float2(c01.x, c01.y);
+        cs[1] = make_float2(c01.z, c01.w);
+        if (np > 2) {
+          const float4 c23 = reinterpret_cast<const float4*>(row)[1];
+          cs[2] = make_float2(c23.x, c23.y);
+          cs[3] = make_float2(c23.z, c23.w);
+        }
       } else {
-        fixed_bf16 = make_uint4(cvt_bf16x2(y[0], y[1]), cvt_bf16x2(y[2], y[3]), cvt_bf16x2(y[4], y[5]),
-                                cvt_bf16x2(y[6], y[7]));
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (e < np) cs[e] = row[e];
       }
-    }
-    for (int s = 0; s < n_slots; ++s) {
-      const size_t off = (((size_t)s * a.H + h) * a.T + t) * a.D + d0;
-      if (!temporal) {
-        if (F8)
-          *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.qrot) + off) = fixed_f8;
-        else
-          *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.qrot) + off) = fixed_bf16;
-        continue;
-      }
-      const int dtq = ctx.t0_cur + f - ctx.t0[s];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (d0 + 2 * e < a.rope.dt) {
-          const float2 r = rot_exact(x[2 * e], x[2 * e + 1], a.rope.tab_t[dtq * (a.rope.dt >> 1) + ((d0 + 2 * e) >> 1)]);
+        if (e < np) {
+          const float2 r = rot_exact(x[2 * e], x[2 * e + 1], cs[e]);
           y[2 * e] = r.x;
           y[2 * e + 1] = r.y;
         }
       }
-      if (F8) {
-        uint2 o;
-        o.x = cvt_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
-        o.y = cvt_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv);
-        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.qrot) + off) = o;
-      } else {
-        uint4 o;
-        o.x = cvt_bf16x2(y[0], y[1]);
-        o.y = cvt_bf16x2(y[2], y[3]);
-        o.z = cvt_bf16x2(y[4], y[5]);
-        o.w = cvt_bf16x2(y[6], y[7]);
-        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.qrot) + off) = o;
-      }
+    }
+    if (F8) {
+      uint2 o;
+      o.x = cvt_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
+      o.y = cvt_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv);
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.qrot) + off) = o;
+    } else {
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.qrot) + off) =
+          make_uint4(cvt_bf16x2(y[0], y[1]), cvt_bf16x2(y[2], y[3]), cvt_bf16x2(y[4], y[5]),
+                     cvt_bf16x2(y[6], y[7]));
     }
   }
 }
@@ -138,14 +170,15 @@ __global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
 }  // namespace
 
 cudaError_t launch_qrot(const QrotArgs& a, cudaStream_t s) {
-  if (a.D != 128) return cudaErrorInvalidValue;
-  long long work = (long long)a.T * a.H * (a.D / 8);
-  long long grid = (work + 255) / 256;
-  if (grid > 148LL * 16) grid = 148LL * 16;
+  if (a.D != 128 || a.T < 1 || a.H < 1 || a.H > 65535) return cudaErrorInvalidValue;
+  if (a.split && (a.f8 || a.rope.dt > a.D / 2)) return cudaErrorInvalidValue;
+  const dim3 grid((a.T + kTokensPerCta - 1) / kTokensPerCta, a.H);
   if (a.f8)
-    qrot_kernel<true><<<(int)grid, 256, 0, s>>>(a);
+    qrot_kernel<true, false><<<grid, 256, 0, s>>>(a);
+  else if (a.split)
+    qrot_kernel<false, true><<<grid, 256, 0, s>>>(a);
   else
-    qrot_kernel<false><<<(int)grid, 256, 0, s>>>(a);
+    qrot_kernel<false, false><<<grid, 256, 0, s>>>(a);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -56,6 +56,7 @@ struct la_cache {
   float query_kp[34] = {};
   int mem_n = 0, mem_head = 0;      // ConvKV ring state
   bool tc = false;
+  bool q_split = false;          // split rotated-query layout (see QrotArgs)
   CUtensorMap tm_q{}, tm_kv{}, tm_cur{}, tm_mem{};
   int num_sms = 148;
   std::vector<cudaEvent_t> prof_start, prof_stop;
@@ -462,6 +463,8 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
   c->rope.F = cfg->frames_per_block;
   c->rope.GH = cfg->grid_h;
   c->rope.GW = cfg->grid_w;
+  c->rope.div_hw = make_fastdiv((uint32_t)(cfg->grid_h * cfg->grid_w));
+  c->rope.div_w = make_fastdiv((uint32_t)cfg->grid_w);
   c->rope.max_t = L.max_t;
   c->rope.tab_t = reinterpret_cast<const float2*>(c->pool + L.rope_t);
   c->rope.tab_h = reinterpret_cast<const float2*>(c->pool + L.rope_h);
@@ -498,7 +501,12 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
   if (st == LA_OK && c->tc) {
     const int H = cfg->num_heads, D = cfg->head_dim;
     const int elt = cfg->kv_dtype == LA_E4M3 ? 1 : 2;
-    bool ok = encode_map(c, &c->tm_q, c->pool + L.qrot, D, c->T, (uint64_t)L.n_qrot * H, elt) &&
+    // bf16 queries whose temporal pairs all sit in the first half of the head
+    // dim: one rotated copy of the first half per slot, the second half once
+    c->q_split = elt == 2 && cfg->rope_t <= D / 2;
+    bool ok = (c->q_split ? encode_map(c, &c->tm_q, c->pool + L.qrot, D / 2, c->T,
+                                       (uint64_t)(L.n_qrot + 1) * H, elt)
+                          : encode_map(c, &c->tm_q, c->pool + L.qrot, D, c->T, (uint64_t)L.n_qrot * H, elt)) &&
               encode_map(c, &c->tm_kv, c->pool + L.frames, D, c->T,
                          (uint64_t)cfg->num_layers * L.n_frames * L.G * H, elt) &&
               encode_map(c, &c->tm_cur, c->pool + L.cur_pages, D, c->T, 2ull * H, elt);
@@ -831,6 +839,7 @@ la_status chunk_attention(la_cache* c, int layer, const void* q, const void* k_c
     qa.D = g.head_dim;
     qa.n_qrot = c->L.n_qrot;
     qa.f8 = g.kv_dtype == LA_E4M3;
+    qa.split = c->q_split;
     qa.qscale = reinterpret_cast<float*>(c->pool + c->L.qscale);
     qa.rope = c->rope;
     qa.err = err;
@@ -843,6 +852,7 @@ la_status chunk_attention(la_cache* c, int layer, const void* q, const void* k_c
     ta.tm_mem = c->tm_mem;
     ta.ctx = dctx;
     ta.kv_f8 = g.kv_dtype == LA_E4M3;
+    ta.q_shared_z = c->q_split ? c->L.n_qrot * g.num_heads : -1;
     ta.frame_scales = ta.kv_f8 ? frame_scales(c, layer, 0) : nullptr;
     ta.cur_scales = reinterpret_cast<const float*>(c->pool + c->L.cur_scales);
     ta.q_scales = reinterpret_cast<const float*>(c->pool + c->L.qscale);

@@ -76,9 +76,24 @@ struct Layout {
   int T;
 };
 
+// Division by a run-time constant d >= 1, for numerators below 2^31, as a
+// multiply-high, an add and a shift (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", 1994): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, n / d = (umulhi(n, m) + n) >> l.
+struct FastDiv {
+  uint32_t d, m, l;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+  return FastDiv{d, (uint32_t)m, l};
+}
+
 struct RopeDims {
   int dt, dh, dw;                  // dims per axis
   int F, GH, GW;                   // block grid
+  FastDiv div_hw, div_w;           // by GH * GW and by GW (token -> frame, row, column)
   int max_t;                       // rows of tab_t
   const float2* tab_t;             // [max_t][dt/2]
   const float2* tab_h;             // [GH][dh/2]
@@ -165,18 +180,22 @@ cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t s);
 
 struct QrotArgs {
   const void* q;       // [T][H][D] bf16
-  void* qrot;          // [S][H][T][D] bf16, or e4m3 codes when f8
+  void* qrot;          // [S][H][T][D] bf16, or e4m3 codes when f8; when split:
+                       // [S+1][H][T][D/2] bf16, dims 0..D/2-1 per slot and
+                       // dims D/2..D-1 (no temporal pair) once, at slot S
   float* qscale;       // f8: [H][T] per-token scales
   const DevContext* ctx;
   int T, H, D, n_qrot;
   int f8;
+  int split;           // bf16 with every temporal dim below D/2 (layout above)
   RopeDims rope;
   DevError* err;
 };
 cudaError_t launch_qrot(const QrotArgs& a, cudaStream_t s);
 
 struct TcAttnArgs {
-  CUtensorMap tm_q;    // rotated queries  [S*H][T][D] bf16 (e4m3 codes when kv_f8)
+  CUtensorMap tm_q;    // rotated queries  [S*H][T][D] bf16 (e4m3 codes when kv_f8),
+                       // or [(S+1)*H][T][D/2] bf16 when q_shared_z >= 0
   CUtensorMap tm_kv;   // pool pages       [frames*G*H][T][D] kv dtype (whole pool)
   CUtensorMap tm_cur;  // current pages    [2*H][T][D]
   CUtensorMap tm_mem;  // ConvKV rings     [L*3*H][cap][D] (or a dummy)
@@ -186,6 +205,8 @@ struct TcAttnArgs {
   const float* q_scales;      // e4m3: [H][T]
   int n_frames;               // frames per layer (bound of ctx->frame)
   int kv_f8;                  // 1: e4m3 K/V and queries, kind::f8f6f4
+  int q_shared_z;             // >= 0: split query rows; the second half of head h's
+                              // rows sits at map z = q_shared_z + h (one copy for all slots)
   uint64_t timeout_ns;        // limit of every wait in the kernel
   int stall;                  // failure injection: the MMA thread first waits on a
                               // barrier nothing completes (runs into timeout_ns)

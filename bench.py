@@ -38,6 +38,35 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+# ------------------------------------------------------------------ ranks
+def init_ranks(backend="nccl"):
+    """(world, rank, local rank) from the torchrun environment; joins the
+    process group when there is more than one rank.  Ranks are replicas: each
+    streams its own blocks, and only the timing is combined."""
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x, device):
+    """The largest value of x over all ranks (the slowest rank's time)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    if dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, t_max):
+    """Units of all ranks over the slowest rank's time."""
+    return units_per_rank * world / t_max
+
+
 def args_():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -490,11 +519,7 @@ def run_ours(a):
     from bounded_kv_cache_la_b300 import build, capi
     from synth import gen
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
+    world, rank, local = init_ranks("nccl")
     torch.cuda.set_device(local)
     if not os.path.exists(capi.LIB_PATH):
         build.build()
@@ -615,12 +640,9 @@ def run_ours(a):
     ctx_kv = context_len(sc)
     flops_call = attn_flops(sc, ctx_kv)
     flops_block = flops_call * S * L
-    t = torch.tensor([elapsed], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    t_max = float(t.item())
-    value = flops_block * a.steps * world / t_max / 1e12
-    blocks_per_s = a.steps * world / t_max
+    t_max = max_over_ranks(elapsed, dev)
+    value = whole_job_rate(flops_block * a.steps, world, t_max) / 1e12
+    blocks_per_s = whole_job_rate(a.steps, world, t_max)
 
     pk, pk_kind = peaks()
     achieved = flops_call / (attn_ms.mean() / 1e3) / 1e12
@@ -704,13 +726,11 @@ def run_ours(a):
             e2e_step()
         barrier()
         e_el = time.perf_counter() - e0
-        te = torch.tensor([e_el], device=dev)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": flops_block * a.e2e_steps * world / float(te.item()) / 1e12,
+        te = max_over_ranks(e_el, dev)
+        e2e = {"value": whole_job_rate(flops_block * a.e2e_steps, world, te) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d // a.e2e_steps,
                "d2h_bytes_per_step": d2h // a.e2e_steps,
-               "blocks_per_s": a.e2e_steps * world / float(te.item()), "steps": a.e2e_steps,
+               "blocks_per_s": whole_job_rate(a.e2e_steps, world, te), "steps": a.e2e_steps,
                "api": "la_select_context + la_fill_block + la_chunk_attention + "
                       "la_cache_append_block, pinned host Q/K/V in and every output back; "
                       "transfers on two copy streams overlapping the attention"}

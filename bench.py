@@ -219,16 +219,18 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9], float(parts[3])))
             except ValueError:
                 continue
         os.unlink(self.f.name)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags) if f == "Active"})
+        reasons = sorted({n for _, _, flags, _ in rows for n, f in zip(names, flags) if f == "Active"})
         return {"sm_mhz": float(np.median([r[0] for r in rows])),
-                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows),
+                "power_w": {"median": float(np.median([r[3] for r in rows])),
+                            "max": max(r[3] for r in rows)}}
 
 
 def kernel_traffic(sc):

@@ -16,8 +16,18 @@ __global__ void init_axis_table(float2* tab, int rows, int d_axis, double theta)
   tab[i] = make_float2((float)cos(ang), (float)sin(ang));
 }
 
+// tab2[i] = (cos, cos, sin, sin) of tab[i]: one 16-byte load gives the
+// packed (c, c) and (s, s) operands that turn two tokens at once.
+__global__ void dup_table(float4* tab2, const float2* tab, int n) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float2 cs = tab[i];
+  tab2[i] = make_float4(cs.x, cs.x, cs.y, cs.y);
+}
+
 cudaError_t launch_init_tables(float2* tab_t, int max_t, int dt, float2* tab_h, int GH, int dh,
-                               float2* tab_w, int GW, int dw, double theta, cudaStream_t s) {
+                               float2* tab_w, int GW, int dw, double theta, float4* tab_t2,
+                               cudaStream_t s) {
   struct { float2* p; int rows; int d; } parts[3] = {{tab_t, max_t, dt}, {tab_h, GH, dh},
                                                      {tab_w, GW, dw}};
   for (auto& pt : parts) {
@@ -27,6 +37,12 @@ cudaError_t launch_init_tables(float2* tab_t, int max_t, int dt, float2* tab_h, 
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+  }
+  const int n_t = max_t * (dt / 2);
+  if (tab_t2 && n_t > 0) {
+    dup_table<<<(n_t + 255) / 256, 256, 0, s>>>(tab_t2, tab_t, n_t);
+    count_launches(1);
+    return cudaGetLastError();
   }
   return cudaSuccess;
 }

@@ -15,35 +15,21 @@ namespace {
 
 using namespace ptx;
 
-// Per-slot rotated copies of the queries: qrot[s][h][t] = R(t0_cur + f - t0_s, row, col) q[t][h].
-// bf16 cache: bf16 copies.  e4m3 cache: e4m3 codes with one fp32 scale per
-// (head, token), qscale[h][t] = m / 448 where m is the largest norm of the
-// token's 64 rotation pairs -- rotations keep pair norms, so one scale
-// serves every slot and no code saturates.
-// SPLIT (bf16, every temporal dim below D/2): the copies hold only the first
-// half of each row; the second half, the same for every slot, is written
-// once at slot index n_qrot.
-//
-// Grid: x = tile of 16 tokens, y = head; one thread per 8 dims.  Full rows:
-// the 16 threads of a token are 16 consecutive lanes.  SPLIT: warps 0-3 take
-// the first halves (8 lanes per token, one store per slot), warps 4-7 the
-// second halves (one store).  Index math is 32-bit and done once per thread;
-// the slot loop only steps the destination and picks the table row.
-constexpr int kTokensPerCta = 16;
+constexpr int kTokensPerCta = 16;       // full rows
+constexpr int kSplitTokensPerCta = 32;  // split rows
 
-template <bool F8, bool SPLIT>
-__global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
-  __shared__ int s_dq[kMaxAttnSlots];                 // t0_cur - t0_s
+// Loads t0_cur - t0_s of every slot into s_dq and checks that each slot's
+// temporal offset stays inside the RoPE table for every frame of the block.
+// Called by every thread of the CTA; false (for all of them) on a bad table.
+__device__ __forceinline__ bool slot_offsets(const QrotArgs& a, int* s_dq) {
   __shared__ int s_bad;
   const DevContext& ctx = *a.ctx;
   const int n_slots = ctx.n_slots;
   if (n_slots < 1 || n_slots > a.n_qrot || n_slots > kMaxAttnSlots) {
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
       record_error(a.err, LA_ERR_DEVICE, KID_QROT, n_slots, a.n_qrot);
-    return;
+    return false;
   }
-  // every slot's temporal offset must stay inside the RoPE table for every
-  // frame of the block (checked up front so that all threads leave together)
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   if ((int)threadIdx.x < n_slots) {
@@ -56,18 +42,27 @@ __global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
     }
   }
   __syncthreads();
-  if (s_bad) return;
+  return s_bad == 0;
+}
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Full rows: qrot[s][h][t] = R(t0_cur + f - t0_s, row, col) q[t][h].
+// bf16 cache: bf16 copies.  e4m3 cache: e4m3 codes with one fp32 scale per
+// (head, token), qscale[h][t] = m / 448 where m is the largest norm of the
+// token's 64 rotation pairs -- rotations keep pair norms, so one scale
+// serves every slot and no code saturates.
+// Grid: x = tile of 16 tokens, y = head; one thread per 8 dims, the 16
+// threads of a token 16 consecutive lanes.  Index math is 32-bit and done
+// once per thread; the slot loop only steps the destination and picks the
+// table row.
+template <bool F8>
+__global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
+  __shared__ int s_dq[kMaxAttnSlots];                 // t0_cur - t0_s
+  if (!slot_offsets(a, s_dq)) return;
+  const int n_slots = a.ctx->n_slots;
+
   const int h = blockIdx.y;
-  int t, cch;
-  if (SPLIT) {
-    t = blockIdx.x * kTokensPerCta + (warp & 3) * 4 + (lane >> 3);
-    cch = (warp >= 4 ? 8 : 0) + (lane & 7);
-  } else {
-    t = blockIdx.x * kTokensPerCta + (threadIdx.x >> 4);
-    cch = threadIdx.x & 15;
-  }
+  const int t = blockIdx.x * kTokensPerCta + (threadIdx.x >> 4);
+  const int cch = threadIdx.x & 15;
   const bool valid = t < a.T;
   float x[8];
   {
@@ -109,15 +104,7 @@ __global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
       y[2 * e + 1] = r.y;
     }
   }
-  const int half = a.D / 2;
-  const int row_len = SPLIT ? half : a.D;
-  if (SPLIT && cch * 8 >= half) {                     // the shared second half
-    const size_t off = (((size_t)a.n_qrot * a.H + h) * a.T + t) * row_len + (d0 - half);
-    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.qrot) + off) =
-        make_uint4(cvt_bf16x2(y[0], y[1]), cvt_bf16x2(y[2], y[3]), cvt_bf16x2(y[4], y[5]),
-                   cvt_bf16x2(y[6], y[7]));
-    return;
-  }
+  const int row_len = a.D;
   const size_t slot_stride = (size_t)a.H * a.T * row_len;
   size_t off = ((size_t)h * a.T + t) * row_len + d0;
   const int pair0 = d0 >> 1, pairs_t = a.rope.dt >> 1;
@@ -167,18 +154,141 @@ __global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
   }
 }
 
+
+// Split rows (bf16, every temporal dim below D/2): each slot gets the first
+// half of every row, turned for that slot; the second half, the same for
+// every slot, is written once at slot index n_qrot.
+// Grid: x = tile of 32 tokens, y = head.  A thread takes 8 dims of two
+// neighbouring tokens a, b: warps 0-3 the first halves, warps 4-7 the
+// second halves.  Tokens a and b normally share a frame, hence a table row:
+// the temporal pairs of both then turn together in packed fp32x2,
+//   y0 = fma(-x1, s, x0 c),  y1 = fma(x0, s, x1 c),
+// with (c, c) and (s, s) from one 16-byte load of the (cos, cos, sin, sin)
+// table; a pair that straddles a frame boundary does the same per token.
+__device__ __forceinline__ void load_row8(const QrotArgs& a, int t, int h, int d0, float* x) {
+  const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) +
+                                                  ((size_t)t * a.H + h) * a.D + d0);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void store_row8(void* base, size_t off, const float* y) {
+  *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + off) =
+      make_uint4(cvt_bf16x2(y[0], y[1]), cvt_bf16x2(y[2], y[3]), cvt_bf16x2(y[4], y[5]),
+                 cvt_bf16x2(y[6], y[7]));
+}
+// Height / width pairs of one token (slot-independent), single roundings.
+__device__ __forceinline__ void turn_static(const QrotArgs& a, int t, int d0, const float* x, float* y) {
+  int f, hh, ww;
+  token_pos(a.rope, t, f, hh, ww);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    y[2 * e] = x[2 * e];
+    y[2 * e + 1] = x[2 * e + 1];
+    if (d0 + 2 * e >= a.rope.dt) {
+      const float2 r = rot_exact(x[2 * e], x[2 * e + 1], rope_cs(a.rope, d0 + 2 * e, 0, hh, ww));
+      y[2 * e] = r.x;
+      y[2 * e + 1] = r.y;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) qrot_split_kernel(QrotArgs a) {
+  __shared__ int s_dq[kMaxAttnSlots];                 // t0_cur - t0_s
+  if (!slot_offsets(a, s_dq)) return;
+  const int n_slots = a.ctx->n_slots;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int ta = blockIdx.x * kSplitTokensPerCta + 2 * ((warp & 3) * 4 + (lane >> 3));
+  const int tb = ta + 1;
+  if (ta >= a.T) return;
+  const bool has_b = tb < a.T;
+  const int half = a.D / 2;
+  const int d0 = (warp >= 4 ? half : 0) + (lane & 7) * 8;
+  float xa[8], xb[8], ya[8], yb[8];
+  load_row8(a, ta, h, d0, xa);
+  if (has_b) load_row8(a, tb, h, d0, xb);
+  else
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xb[e] = 0.f;
+  turn_static(a, ta, d0, xa, ya);
+  turn_static(a, has_b ? tb : ta, d0, xb, yb);
+  const size_t row_a = ((size_t)h * a.T + ta) * half;   // row of token a in one copy
+  if (d0 >= half) {                                    // the shared second half, once
+    const size_t off = (size_t)a.n_qrot * a.H * a.T * half + row_a + (d0 - half);
+    store_row8(a.qrot, off, ya);
+    if (has_b) store_row8(a.qrot, off + half, yb);
+    return;
+  }
+  const int fa = (int)fdiv((uint32_t)ta, a.rope.div_hw);
+  const int fb = has_b ? (int)fdiv((uint32_t)tb, a.rope.div_hw) : fa;
+  const int pairs_t = a.rope.dt >> 1, pair0 = d0 >> 1;
+  const int np = min(max((a.rope.dt - d0) >> 1, 0), 4);   // temporal pairs here
+  // packed (token a, token b) operands of the temporal pairs
+  float2 x0[4], x1[4], nx1[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x0[e] = make_float2(xa[2 * e], xb[2 * e]);
+    x1[e] = make_float2(xa[2 * e + 1], xb[2 * e + 1]);
+    nx1[e] = make_float2(-xa[2 * e + 1], -xb[2 * e + 1]);
+  }
+  const size_t slot_stride = (size_t)a.H * a.T * half;
+  size_t off = row_a + d0;
+#pragma unroll 2
+  for (int s = 0; s < n_slots; ++s, off += slot_stride) {
+    if (np > 0) {
+      if (fa == fb) {
+        const float4* row = a.rope.tab_t2 + (size_t)(s_dq[s] + fa) * pairs_t + pair0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e < np) {
+            const float4 cs = row[e];
+            const float2 c = make_float2(cs.x, cs.y), sn = make_float2(cs.z, cs.w);
+            const float2 y0 = ffma2(nx1[e], sn, fmul2(x0[e], c));
+            const float2 y1 = ffma2(x0[e], sn, fmul2(x1[e], c));
+            ya[2 * e] = y0.x; yb[2 * e] = y0.y;
+            ya[2 * e + 1] = y1.x; yb[2 * e + 1] = y1.y;
+          }
+        }
+      } else {                                         // a and b in different frames
+        const float2* ra = a.rope.tab_t + (size_t)(s_dq[s] + fa) * pairs_t + pair0;
+        const float2* rb = a.rope.tab_t + (size_t)(s_dq[s] + fb) * pairs_t + pair0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e < np) {
+            const float2 ca = ra[e], cb = rb[e];
+            ya[2 * e] = fmaf(-xa[2 * e + 1], ca.y, __fmul_rn(xa[2 * e], ca.x));
+            ya[2 * e + 1] = fmaf(xa[2 * e], ca.y, __fmul_rn(xa[2 * e + 1], ca.x));
+            yb[2 * e] = fmaf(-xb[2 * e + 1], cb.y, __fmul_rn(xb[2 * e], cb.x));
+            yb[2 * e + 1] = fmaf(xb[2 * e], cb.y, __fmul_rn(xb[2 * e + 1], cb.x));
+          }
+        }
+      }
+    }
+    store_row8(a.qrot, off, ya);
+    if (has_b) store_row8(a.qrot, off + half, yb);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_qrot(const QrotArgs& a, cudaStream_t s) {
   if (a.D != 128 || a.T < 1 || a.H < 1 || a.H > 65535) return cudaErrorInvalidValue;
   if (a.split && (a.f8 || a.rope.dt > a.D / 2)) return cudaErrorInvalidValue;
-  const dim3 grid((a.T + kTokensPerCta - 1) / kTokensPerCta, a.H);
-  if (a.f8)
-    qrot_kernel<true, false><<<grid, 256, 0, s>>>(a);
-  else if (a.split)
-    qrot_kernel<false, true><<<grid, 256, 0, s>>>(a);
-  else
-    qrot_kernel<false, false><<<grid, 256, 0, s>>>(a);
+  if (a.split && !a.rope.tab_t2) return cudaErrorInvalidValue;
+  if (a.split) {
+    const dim3 grid((a.T + kSplitTokensPerCta - 1) / kSplitTokensPerCta, a.H);
+    qrot_split_kernel<<<grid, 256, 0, s>>>(a);
+  } else {
+    const dim3 grid((a.T + kTokensPerCta - 1) / kTokensPerCta, a.H);
+    if (a.f8)
+      qrot_kernel<true><<<grid, 256, 0, s>>>(a);
+    else
+      qrot_kernel<false><<<grid, 256, 0, s>>>(a);
+  }
   count_launches(1);
   return cudaGetLastError();
 }

@@ -183,6 +183,7 @@ void compute_layout(const la_cache_config& c, Layout& L) {
   const bool f8 = c.kv_dtype == LA_E4M3;
   L.qrot = take(tc ? (size_t)L.n_qrot * H * T * D * (f8 ? 1 : 2) : 0);
   L.qscale = take(tc && f8 ? sizeof(float) * (size_t)H * T : 0);
+  L.rope_t2 = take(tc && !f8 ? sizeof(float4) * (size_t)L.max_t * (c.rope_t / 2 > 0 ? c.rope_t / 2 : 1) : 0);
   L.mem = take(is_prsink(c) ? 0 : (size_t)c.num_layers * 3 * H * c.mem_slots * D * 2);
   L.total = off;
 }
@@ -467,6 +468,9 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
   c->rope.div_w = make_fastdiv((uint32_t)cfg->grid_w);
   c->rope.max_t = L.max_t;
   c->rope.tab_t = reinterpret_cast<const float2*>(c->pool + L.rope_t);
+  c->rope.tab_t2 = tc_eligible(*cfg, L) && cfg->kv_dtype != LA_E4M3
+                       ? reinterpret_cast<const float4*>(c->pool + L.rope_t2)
+                       : nullptr;
   c->rope.tab_h = reinterpret_cast<const float2*>(c->pool + L.rope_h);
   c->rope.tab_w = reinterpret_cast<const float2*>(c->pool + L.rope_w);
   const int hist = is_prsink(*cfg) ? cfg->max_history : 1;
@@ -488,7 +492,8 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
                                         cfg->rope_t, reinterpret_cast<float2*>(c->pool + L.rope_h),
                                         cfg->grid_h, cfg->rope_h,
                                         reinterpret_cast<float2*>(c->pool + L.rope_w), cfg->grid_w,
-                                        cfg->rope_w, (double)cfg->rope_theta, s),
+                                        cfg->rope_w, (double)cfg->rope_theta,
+                                        const_cast<float4*>(c->rope.tab_t2), s),
                      "rope tables");
   if (st == LA_OK && cfg->kv_dtype == LA_E4M3)
     st = cuda_status(c, cudaMemsetAsync(c->pool + L.scales, 0, L.frames - L.scales, s),

@@ -64,6 +64,7 @@ struct Layout {
   size_t frames;                   // [L][n_frames][G] pages
   size_t cur_pages;                // 2 pages: current block K', V
   size_t qrot;                     // [S][H][T][D] rotated queries (tensor path), kv dtype
+  size_t rope_t2;                  // bf16 tensor path: temporal table as (cos, cos, sin, sin)
   size_t qscale;                   // e4m3 tensor path: [H][T] fp32 query scales
   size_t mem;                      // ConvKV [L][3][H][cap][D] bf16 (raw K, V, rotated K)
   size_t total;
@@ -96,6 +97,7 @@ struct RopeDims {
   FastDiv div_hw, div_w;           // by GH * GW and by GW (token -> frame, row, column)
   int max_t;                       // rows of tab_t
   const float2* tab_t;             // [max_t][dt/2]
+  const float4* tab_t2;            // [max_t][dt/2] (cos, cos, sin, sin), or null
   const float2* tab_h;             // [GH][dh/2]
   const float2* tab_w;             // [GW][dw/2]
 };
@@ -106,7 +108,8 @@ void count_launches(int n);
 // ------------------------------------------------------------ kernel launches
 // Each returns the cudaError_t of its launch(es).
 cudaError_t launch_init_tables(float2* tab_t, int max_t, int dt, float2* tab_h, int GH, int dh,
-                               float2* tab_w, int GW, int dw, double theta, cudaStream_t s);
+                               float2* tab_w, int GW, int dw, double theta, float4* tab_t2,
+                               cudaStream_t s);
 
 struct RetrievalArgs {
   float kp[34];

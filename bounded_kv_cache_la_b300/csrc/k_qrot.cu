@@ -196,7 +196,9 @@ __device__ __forceinline__ void turn_static(const QrotArgs& a, int t, int d0, co
   }
 }
 
-__global__ void __launch_bounds__(256) qrot_split_kernel(QrotArgs a) {
+// 4 CTAs per SM (at most 64 registers) keep more Q loads in flight: 62.6 vs
+// 65.1 us per 14B-shape call with the compiler's own 74 registers.
+__global__ void __launch_bounds__(256, 4) qrot_split_kernel(QrotArgs a) {
   __shared__ int s_dq[kMaxAttnSlots];                 // t0_cur - t0_s
   if (!slot_offsets(a, s_dq)) return;
   const int n_slots = a.ctx->n_slots;

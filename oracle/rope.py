@@ -32,11 +32,13 @@ def block_positions(F: int, GH: int, GW: int):
     return f.reshape(-1), h.reshape(-1), w.reshape(-1)
 
 
-def rotate(x: np.ndarray, t, h, w, theta: float = 10000.0) -> np.ndarray:
-    """Rotate x [N, ..., D] by per-token positions t, h, w (each [N]); fp64."""
+def rotate(x: np.ndarray, t, h, w, theta: float = 10000.0, parts=None) -> np.ndarray:
+    """Rotate x [N, ..., D] by per-token positions t, h, w (each [N]); fp64.
+    parts: the (t, h, w) dims of the head dim, default split(D)."""
     x = np.asarray(x, dtype=np.float64)
     D = x.shape[-1]
-    parts = split(D)
+    parts = split(D) if parts is None else tuple(parts)
+    assert sum(parts) == D and all(d % 2 == 0 for d in parts)
     out = x.copy()
     base = 0
     for pos, d in zip((t, h, w), parts):

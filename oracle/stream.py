@@ -87,6 +87,13 @@ def plan_stream(cfg, kps: np.ndarray, n_blocks: int | None = None) -> list[Conte
 
 
 # ------------------------------------------------------------ value handling
+def rope_parts(cfg) -> tuple[int, int, int]:
+    """(t, h, w) dims of the head dim: the config's explicit split when it
+    gives one (the C ABI takes any even split), else rope.split(D)."""
+    dims = getattr(cfg, "rope_dims", None)
+    return tuple(dims) if dims else rope.split(cfg.head_dim)
+
+
 def rotate_within_block_f32(x: np.ndarray, cfg) -> np.ndarray:
     """Key rotated by its within-block (frame, row, column) position using
     fp32 single roundings: each product and the sum/difference rounded once,
@@ -95,7 +102,7 @@ def rotate_within_block_f32(x: np.ndarray, cfg) -> np.ndarray:
     f, h, w = rope.block_positions(cfg.frames_per_block, cfg.grid_h, cfg.grid_w)
     out = x.copy()
     base = 0
-    for pos, d in zip((f, h, w), rope.split(cfg.head_dim)):
+    for pos, d in zip((f, h, w), rope_parts(cfg)):
         ang = pos.astype(np.float64)[:, None] * rope.freqs(d, cfg.rope_theta)[None, :]
         c = np.cos(ang).astype(np.float32)[:, None, :]
         s = np.sin(ang).astype(np.float32)[:, None, :]
@@ -136,7 +143,7 @@ def context_kv(cfg, ctx: Context, kv_of, mem=None):
         assert km.shape[0] == ctx.mem_tokens
         j = np.arange(ctx.mem_tokens)
         z = np.zeros_like(j)
-        ks.append(rope.rotate(km, j, z, z, cfg.rope_theta))
+        ks.append(rope.rotate(km, j, z, z, cfg.rope_theta, rope_parts(cfg)))
         vs.append(np.asarray(vm, dtype=np.float64))
     for blk, t0 in zip(ctx.blocks, ctx.t0):
         k, v = kv_of(blk)
@@ -144,10 +151,10 @@ def context_kv(cfg, ctx: Context, kv_of, mem=None):
             _, _, kd, _ = fp8_store(rotate_within_block_f32(k, cfg))
             _, _, vd, _ = fp8_store(np.asarray(v, dtype=np.float32))
             zero = np.zeros_like(f)
-            ks.append(rope.rotate(kd, t0 + zero, zero, zero, cfg.rope_theta))
+            ks.append(rope.rotate(kd, t0 + zero, zero, zero, cfg.rope_theta, rope_parts(cfg)))
             vs.append(vd)
         else:
-            ks.append(rope.rotate(k, t0 + f, h, w, cfg.rope_theta))
+            ks.append(rope.rotate(k, t0 + f, h, w, cfg.rope_theta, rope_parts(cfg)))
             vs.append(np.asarray(v, dtype=np.float64))
     return np.concatenate(ks, axis=0), np.concatenate(vs, axis=0)
 
@@ -162,7 +169,8 @@ def chunk_attention(cfg, ctx: Context, q: np.ndarray, kv_of, mem=None, rows=None
     if rows is None:
         rows = np.arange(q.shape[0])
     rows = np.asarray(rows)
-    qr = rope.rotate(np.asarray(q)[rows], t0c + f[rows], h[rows], w[rows], cfg.rope_theta)
+    qr = rope.rotate(np.asarray(q)[rows], t0c + f[rows], h[rows], w[rows], cfg.rope_theta,
+                     rope_parts(cfg))
     K, V = context_kv(cfg, ctx, kv_of, mem)
     out = np.zeros((len(rows), q.shape[1], V.shape[2]))
     for hh in range(q.shape[1]):

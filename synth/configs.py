@@ -52,6 +52,7 @@ class StreamConfig:
     rope_theta: float = 10000.0
     history_mode: str = "resident"   # "resident" | "external"
     seed: int = 0
+    rope_dims: tuple | None = None   # explicit (t, h, w) split of the head dim
 
     @property
     def tokens_per_block(self) -> int:
@@ -67,7 +68,10 @@ class StreamConfig:
 
     @property
     def rope_split(self) -> tuple[int, int, int]:
-        """Head-dim split into (t, h, w) rotary parts: w = h = 2*floor(D/6)."""
+        """Head-dim split into (t, h, w) rotary parts: w = h = 2*floor(D/6)
+        unless rope_dims gives one."""
+        if self.rope_dims:
+            return tuple(self.rope_dims)
         d = self.head_dim
         hw = 2 * (d // 6)
         return d - 2 * hw, hw, hw

@@ -227,3 +227,39 @@ def test_largest_dynamic_sink():
             continue
         o = H.oracle_output(sc, ctx, vals, 0, 0, 1)
         H.compare(outs[b][(0, 0)], o, "bf16", f"block {b}")
+
+
+def _all_rows_against_oracle(sc, n, keep, tol):
+    _, ctxs, outs = H.run_stream(sc, n, keep, attn_impl=1)
+    ref = ostream.plan_stream(sc, gen.poses(sc, n_blocks=n), n)
+    vals = H.Values(sc)
+    checked = 0
+    for b in sorted(keep):
+        ctx = ref[b]
+        assert ctxs[b]["kv_len"] == ctx.kv_len
+        if ctxs[b]["dyn_ids"] != ctx.dyn_ids:
+            assert ctx.gap <= 1e-6
+            continue
+        o = H.oracle_output(sc, ctx, vals, 0, 0, 1)
+        H.compare(outs[b][(0, 0)], o, tol, f"block {b}")
+        checked += 1
+    assert checked >= len(keep) - 1
+
+
+def test_odd_frame_and_block_sizes():
+    """Frames of 5 x 7 tokens and 105 tokens per block, both odd: the query
+    rotation's token pairs that straddle a frame boundary and a last token
+    without a partner; all rows against the oracle."""
+    sc = C2_MID.with_(num_heads=3, frames_per_block=3, grid_h=5, grid_w=7)
+    _all_rows_against_oracle(sc, 10, {0, 4, 6, 9}, "bf16")
+
+
+@pytest.mark.parametrize("dims,kv", [((72, 28, 28), "bf16"), ((70, 30, 28), "bf16"),
+                                     ((42, 44, 42), "bf16"), ((42, 44, 42), "e4m3")])
+def test_other_rope_splits(dims, kv):
+    """Other (t, h, w) splits of the head dim: a temporal part wider than half
+    a row (whole-row query copies), one that is not a multiple of 4 (pairs
+    read one at a time), and the e4m3 path; all rows against the oracle."""
+    sc = C2_MID.with_(num_heads=2, frames_per_block=2, grid_h=6, grid_w=9, rope_dims=dims,
+                      kv_dtype=kv)
+    _all_rows_against_oracle(sc, 8, {0, 4, 7}, "bf16" if kv == "bf16" else "e4m3_tc")

@@ -15,13 +15,13 @@ def test_split_sizes():
     assert rope.split(128) == (44, 42, 42)
 
 
-def _rotate_complex(x, t, h, w, theta=10000.0):
+def _rotate_complex(x, t, h, w, theta=10000.0, parts=None):
     """Independent formulation: each (2i, 2i+1) pair is a complex number
     multiplied by exp(i * pos * theta^(-2i/d))."""
     D = x.shape[-1]
     out = np.empty_like(x, dtype=np.float64)
     base = 0
-    for pos, d in zip((t, h, w), rope.split(D)):
+    for pos, d in zip((t, h, w), parts or rope.split(D)):
         z = x[..., base:base + d:2] + 1j * x[..., base + 1:base + d:2]
         i = np.arange(d // 2)
         ang = np.asarray(pos, dtype=np.float64)[:, None] * np.power(theta, -2.0 * i / d)[None, :]
@@ -39,6 +39,20 @@ def test_rotate_matches_complex_multiplication():
         t, h, w = (rng.integers(0, 60, size=37) for _ in range(3))
         np.testing.assert_allclose(rope.rotate(x, t, h, w), _rotate_complex(x, t, h, w),
                                    rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("parts", [(72, 28, 28), (42, 44, 42), (70, 30, 28), (128, 0, 0)])
+def test_rotate_explicit_split_matches_complex_multiplication(parts):
+    # the C ABI takes any even (t, h, w) split of the head dim
+    rng = np.random.default_rng(1)
+    x = rng.normal(size=(29, 128))
+    t, h, w = (rng.integers(0, 60, size=29) for _ in range(3))
+    np.testing.assert_allclose(rope.rotate(x, t, h, w, parts=parts),
+                               _rotate_complex(x, t, h, w, parts=parts), rtol=0, atol=1e-12)
+    # only the temporal part moves when h = w = 0
+    z = np.zeros_like(t)
+    y = rope.rotate(x, t, z, z, parts=parts)
+    np.testing.assert_array_equal(y[:, parts[0]:], x[:, parts[0]:])
 
 
 def test_rotate_closed_form_small():

@@ -79,6 +79,7 @@ struct Range {
 };
 
 constexpr size_t kAlign = 1024;
+constexpr long long kMaxBlockTokens = 1 << 20;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int elt_size(int dtype) { return dtype == LA_F32 ? 4 : dtype == LA_BF16 ? 2 : 1; }
@@ -91,6 +92,9 @@ la_status validate(const la_cache_config* c) {
   if (c->num_layers < 1 || c->num_heads < 1 || c->num_heads > 64) return LA_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return LA_ERR_UNSUPPORTED;
   if (c->frames_per_block < 1 || c->grid_h < 1 || c->grid_w < 1) return LA_ERR_INVALID_ARG;
+  // token indices are 32-bit in the kernels (divided by multiply-high below 2^31)
+  if ((long long)c->frames_per_block * c->grid_h * c->grid_w > kMaxBlockTokens)
+    return LA_ERR_UNSUPPORTED;
   if (c->rope_t < 0 || c->rope_h < 0 || c->rope_w < 0 || (c->rope_t | c->rope_h | c->rope_w) & 1 ||
       c->rope_t + c->rope_h + c->rope_w != c->head_dim)
     return LA_ERR_INVALID_ARG;

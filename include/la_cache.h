@@ -70,7 +70,7 @@ typedef enum { LA_ATTN_AUTO = 0, LA_ATTN_TENSOR = 1, LA_ATTN_SIMT = 2 } la_attn_
 
 typedef struct {
   int32_t num_layers, num_heads, head_dim;       /* L, H, D (D = 64 or 128)           */
-  int32_t frames_per_block, grid_h, grid_w;      /* T = F * GH * GW tokens per block  */
+  int32_t frames_per_block, grid_h, grid_w;      /* T = F * GH * GW <= 2^20 tokens    */
   int32_t rope_t, rope_h, rope_w;                /* RoPE dims per axis, sum = D       */
   float   rope_theta;                            /* 10000                              */
   int32_t policy;                                /* la_policy                          */

@@ -65,6 +65,9 @@ def test_invalid_configs_rejected():
     cfg = capi.config_for(C2_MID)
     cfg.head_dim = 96
     assert capi.la_cache_required_bytes(cfg) == 0
+    cfg = capi.config_for(C2_MID)
+    cfg.grid_h, cfg.grid_w = 1024, 1025           # 2 x 1024 x 1025 tokens per block
+    assert capi.la_cache_required_bytes(cfg) == 0
 
 
 @pytest.mark.parametrize("sc,n", [(C1_TINY, 24), (C2_MID, 64), (C3_14B, 400), (C5_FP8, 300)])

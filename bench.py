@@ -160,6 +160,35 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
+def blas_threads():
+    """Threads NumPy's BLAS runs with (what the oracle's matmuls use)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p["num_threads"] for p in threadpool_info() if p.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline():
+    """The oracle on the host cores: the bounded 14B-shape sample with every
+    BLAS thread, and a smaller sample on one thread."""
+    smp = OracleSample(workload())
+    dt = min(smp.run() for _ in range(2))
+    out = {"value": smp.flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+           "kind": "oracle", "sample": smp.text, "seconds": dt}
+    try:
+        from threadpoolctl import threadpool_limits
+        one = OracleSample(workload(), n_heads=2, n_rows=256)
+        with threadpool_limits(limits=1, user_api="blas"):
+            dt1 = one.run()
+        out["single_thread"] = {"value": one.flops / dt1 / 1e12, "cores": 1, "sample": one.text,
+                                "seconds": dt1}
+    except ImportError:
+        pass
+    return out
+
+
 def run_reference(a):
     """Reference arm: the CPU oracle as it stands, on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -173,7 +202,7 @@ def run_reference(a):
     flops, text = smp.flops, smp.text
     tot = sum(times)
     value = flops * a.steps / tot / 1e12
-    cores = os.cpu_count()
+    cores = blas_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
@@ -747,10 +776,7 @@ def run_ours(a):
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline and a.workload == "c3_14b":
-        smp = OracleSample(workload())
-        dt = min(smp.run() for _ in range(2))
-        cpu = {"value": smp.flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
-               "kind": "oracle", "sample": smp.text, "seconds": dt}
+        cpu = cpu_baseline()
 
     if rank == 0:
         traffic = kernel_traffic(sc)

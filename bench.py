@@ -81,6 +81,7 @@ def args_():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the FP8, ConvKV and latency-flatness legs")
     ap.add_argument("--layers", type=int, default=None, help="override (testing only)")
+    ap.add_argument("--oracle-one-thread", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -167,24 +168,39 @@ def blas_threads():
         n = [p["num_threads"] for p in threadpool_info() if p.get("user_api") == "blas"]
         return max(n) if n else 1
     except Exception:
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            if os.environ.get(var, "").isdigit():
+                return int(os.environ[var])
         return os.cpu_count()
+
+
+ONE_THREAD_ENV = {"OPENBLAS_NUM_THREADS": "1", "OMP_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+
+
+def oracle_one_thread():
+    """Child-process entry (--oracle-one-thread): a smaller sample on one BLAS
+    thread; prints its JSON."""
+    one = OracleSample(workload(), n_heads=2, n_rows=256)
+    dt = one.run()
+    print(json.dumps({"value": one.flops / dt / 1e12, "cores": blas_threads(), "sample": one.text,
+                      "seconds": dt}), flush=True)
 
 
 def cpu_baseline():
     """The oracle on the host cores: the bounded 14B-shape sample with every
-    BLAS thread, and a smaller sample on one thread."""
+    BLAS thread, and (in a child process whose BLAS is limited to one thread
+    before NumPy loads) a smaller sample on one thread."""
     smp = OracleSample(workload())
     dt = min(smp.run() for _ in range(2))
     out = {"value": smp.flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
            "kind": "oracle", "sample": smp.text, "seconds": dt}
     try:
-        from threadpoolctl import threadpool_limits
-        one = OracleSample(workload(), n_heads=2, n_rows=256)
-        with threadpool_limits(limits=1, user_api="blas"):
-            dt1 = one.run()
-        out["single_thread"] = {"value": one.flops / dt1 / 1e12, "cores": 1, "sample": one.text,
-                                "seconds": dt1}
-    except ImportError:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-thread"],
+                           capture_output=True, text=True, timeout=300,
+                           env=dict(os.environ, **ONE_THREAD_ENV))
+        if r.returncode == 0 and r.stdout.strip():
+            out["single_thread"] = json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.TimeoutExpired, ValueError, OSError):
         pass
     return out
 
@@ -814,7 +830,9 @@ def run_ours(a):
 
 def main():
     a = args_()
-    if a.impl == "reference":
+    if a.oracle_one_thread:
+        oracle_one_thread()
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)

@@ -82,6 +82,9 @@ def args_():
                     help="skip the FP8, ConvKV and latency-flatness legs")
     ap.add_argument("--layers", type=int, default=None, help="override (testing only)")
     ap.add_argument("--oracle-one-thread", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--full-stream", action="store_true",
+                    help="per-block latency over every block of the 14B and FP8 streams at one layer")
+    ap.add_argument("--full-stream-blocks", type=int, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -560,6 +563,60 @@ def extra_legs(torch, capi, gen, q, k, v, out, bank, main_block_ms, pk):
 
 
 # ------------------------------------------------------------------ our arm
+def full_stream(a):
+    """Per-block latency over every block of the 14B-shape stream (3600
+    blocks) and of the FP8 stress stream (10000 blocks), from block 0, at one
+    layer (all heads, every denoising step, retrieval, fills and appends):
+    the cache's state stays bounded, so the per-block cost must stay flat.
+    Prints one JSON line (not the benchmark line)."""
+    import torch
+    from bounded_kv_cache_la_b300 import build, capi
+    from synth import gen
+
+    if not os.path.exists(capi.LIB_PATH):
+        build.build()
+    torch.cuda.set_device(0)
+    res = {}
+    for name in ("c3_14b", "c5_fp8"):
+        sc = workload(name).with_(num_layers=1)
+        T, H, D = sc.tokens_per_block, sc.num_heads, sc.head_dim
+        g = torch.Generator(device="cuda")
+        g.manual_seed(7)
+
+        def randn():
+            return torch.randn((T, H, D), generator=g, device="cuda").to(torch.bfloat16)
+
+        q = [randn() for _ in range(4)]
+        k = [randn() for _ in range(4)]
+        v = [randn() for _ in range(4)]
+        outs = [torch.empty_like(q[0])]
+        bank = [[(randn(), randn()) for _ in range(4)]]
+        n = sc.n_blocks if a.full_stream_blocks is None else min(sc.n_blocks, a.full_stream_blocks)
+        leg = StreamLeg(torch, capi, gen, sc, 0, n, q, k, v, outs, bank)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        ev[0].record()
+        for i in range(n):
+            leg.step()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        st, msg = leg.cache.la_get_error()
+        if st != capi.LA_OK:
+            raise RuntimeError(msg)
+        ms = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(n)])
+        steady = ms[10:]
+        med = float(np.median(steady))
+        dev = np.abs(steady / med - 1.0)
+        res[name] = {"blocks": n, "layers": 1, "heads": H, "kv_len_steady": context_len(sc),
+                     "median_block_ms": med, "p99_block_ms": float(np.percentile(steady, 99)),
+                     "max_block_ms": float(steady.max()), "max_dev_from_median": float(dev.max()),
+                     "frac_within_5pct": float((dev <= 0.05).mean()),
+                     "first_10_blocks_ms": [round(float(x), 3) for x in ms[:10]],
+                     "median_by_tenth": [round(float(np.median(c)), 3)
+                                         for c in np.array_split(steady, 10)]}
+        leg.close()
+    print(json.dumps({"full_stream_flatness": res}), flush=True)
+
+
 def run_ours(a):
     import torch
     import torch.distributed as dist
@@ -832,6 +889,8 @@ def main():
     a = args_()
     if a.oracle_one_thread:
         oracle_one_thread()
+    elif a.full_stream:
+        full_stream(a)
     elif a.impl == "reference":
         run_reference(a)
     else:

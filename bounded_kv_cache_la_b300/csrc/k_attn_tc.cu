@@ -23,7 +23,7 @@
 // unit are the ones that got fewer full units.
 //
 // CTA = 12 warps, persistent:
-//   warp 0       TMA producer (K ring, V ring, per-slot Q tiles)
+//   warp 0       TMA producer (K ring, V ring, per-slot Q boxes, double-buffered)
 //   warp 1       MMA issuer: S_i = Q_i K^T (smem x smem) into TMEM,
 //                O_i += P_i V (P from TMEM, V from smem, MN-major)
 //   warp 2       TMEM allocator
@@ -82,11 +82,17 @@ struct Tile {
   static constexpr int kBoxElems = 128 / kElt;            // elements per 128-byte row
   static constexpr int kMmaK = F8 ? 32 : 16;              // K of one MMA instruction
   static constexpr int kSteps = kD / kMmaK;               // MMAs per 128-deep product
+  // Query region, in 16 KB boxes: the slot-dependent box of each of the two
+  // tiles, double-buffered (boxes 0-3: buffer b, tile i at 2b + i); bf16
+  // adds the second 64-dim box of each tile (boxes 4-5), which is the same
+  // for every slot when the rotated queries are split.
+  static constexpr int kQBoxes = F8 ? 4 : 6;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kBytes;
+  static constexpr int kOffK = kOffQ + kQBoxes * kBoxBytes;
   static constexpr int kOffV = kOffK + kKSt * kBytes;
   static constexpr int kOffCtl = kOffV + kVSt * kBytes;
   static constexpr int kSmem = kOffCtl + kCtlBytes + 1024; // + alignment slack
+  static_assert(kSmem <= 227 * 1024, "over the per-block shared memory limit");
 };
 constexpr float kRescaleThreshold = 8.0f;                 // log2(256)
 // Measured at the 14B shape (one call, B300): 0 -> 2.75 ms, 4 -> 2.91,
@@ -103,7 +109,8 @@ constexpr uint32_t kP0 = 0x3f7ffb49u, kP1 = 0x3f31798du, kP2 = 0x3e786f0du, kP3 
 constexpr float kRoundMagic = 12582912.0f;                // 1.5 * 2^23
 
 struct Ctl {
-  uint64_t q_full, q_empty;
+  uint64_t q0_full[2], q0_empty[2];   // slot-dependent query boxes, per buffer
+  uint64_t q1_full, q1_empty;         // bf16: second query boxes (per unit when split)
   uint64_t k_full[kKSt], k_empty[kKSt];
   uint64_t v_full[kVSt], v_empty[kVSt];
   uint64_t s_full[2], p_ready[2], o_full[2];
@@ -219,8 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                  sV = smem_u32(smem + Tl::kOffV);
 
   if (tid == 0) {
-    mbar_init(smem_u32(&ctl.q_full), 1);
-    mbar_init(smem_u32(&ctl.q_empty), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctl.q0_full[i]), 1);
+      mbar_init(smem_u32(&ctl.q0_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&ctl.q1_full), 1);
+    mbar_init(smem_u32(&ctl.q1_empty), 1);
     for (int i = 0; i < kKSt; ++i) {
       mbar_init(smem_u32(&ctl.k_full[i]), 1);
       mbar_init(smem_u32(&ctl.k_empty[i]), 1);
@@ -275,8 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
    } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t kc = 0, vc = 0, qc = 0;
+      uint32_t kc = 0, vc = 0, qc = 0, q1c = 0;
       bool ok = true;
+      const bool split = a.q_shared_z >= 0;
       for (int i = 0; ok; ++i) {
         const int u = units.index(i);
         if (u >= units.n_units) break;
@@ -298,17 +310,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                           krow, smem_u32(&ctl.k_full[ks]));
             ++kc;
             if (kt == 0) {
-              if (!(ok = wait(ctl.q_empty, (qc & 1) ^ 1, 2))) break;
-              mbar_arrive_expect_tx(smem_u32(&ctl.q_full), n_qt * Tl::kBytes);
+              // slot s's own query box (dims 0-63 for bf16, the whole row for
+              // e4m3) into the buffer the slot before last used: it loads while
+              // the previous slot is still being computed
+              const int qb = qc & 1;
+              if (!(ok = wait(ctl.q0_empty[qb], ((qc >> 1) & 1) ^ 1, 2))) break;
+              mbar_arrive_expect_tx(smem_u32(&ctl.q0_full[qb]), n_qt * Tl::kBoxBytes);
               for (int qi = 0; qi < n_qt; ++qi)
-                for (int bx = 0; bx < Tl::kBoxes; ++bx) {
-                  // split rows: box 1 is the slot-independent half, one copy per head
-                  const bool sh = a.q_shared_z >= 0 && bx == 1;
-                  tma_load_3d(sQ + qi * Tl::kBytes + bx * Tl::kBoxBytes, &a.tm_q,
-                              a.q_shared_z >= 0 ? 0 : bx * Tl::kBoxElems, row0 + qi * kBM,
-                              sh ? a.q_shared_z + h : s * a.H + h, smem_u32(&ctl.q_full));
-                }
+                tma_load_3d(sQ + (2 * qb + qi) * Tl::kBoxBytes, &a.tm_q, 0, row0 + qi * kBM, s * a.H + h,
+                            smem_u32(&ctl.q0_full[qb]));
               ++qc;
+              // bf16 dims 64-127: once per unit when split (the same rows for
+              // every slot), else with every slot
+              if (!F8 && (!split || s == 0)) {
+                if (!(ok = wait(ctl.q1_empty, (q1c & 1) ^ 1, 4))) break;
+                mbar_arrive_expect_tx(smem_u32(&ctl.q1_full), n_qt * Tl::kBoxBytes);
+                for (int qi = 0; qi < n_qt; ++qi)
+                  tma_load_3d(sQ + (4 + qi) * Tl::kBoxBytes, &a.tm_q, split ? 0 : Tl::kBoxElems,
+                              row0 + qi * kBM, split ? a.q_shared_z + h : s * a.H + h,
+                              smem_u32(&ctl.q1_full));
+                ++q1c;
+              }
             }
             const int vs = vc % kVSt;
             if (!(ok = wait(ctl.v_empty[vs], ((vc / kVSt) & 1) ^ 1, 3))) break;
@@ -331,10 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const uint64_t t0 = globaltimer();
         while (!mbar_try_wait(b, (i / kVSt) & 1) && globaltimer() - t0 < limit_ns) {}
       }
-      if (qc > 0) {
-        const uint32_t b = smem_u32(&ctl.q_full);
+      for (uint32_t i = (qc > 2 ? qc - 2 : 0); i < qc; ++i) {
+        const uint32_t b = smem_u32(&ctl.q0_full[i & 1]);
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(b, (qc - 1) & 1) && globaltimer() - t0 < limit_ns) {}
+        while (!mbar_try_wait(b, (i >> 1) & 1) && globaltimer() - t0 < limit_ns) {}
+      }
+      if (q1c > 0) {
+        const uint32_t b = smem_u32(&ctl.q1_full);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(b, (q1c - 1) & 1) && globaltimer() - t0 < limit_ns) {}
       }
     }
   } else if (warp == 1) {
@@ -342,8 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (lane == 0) {
       const uint32_t idesc_qk = F8 ? idesc_e4m3(kBM, kBN, 0, 0) : idesc_bf16(kBM, kBN, 0, 0);
       const uint32_t idesc_pv = F8 ? idesc_e4m3(kBM, kD, 0, 1) : idesc_bf16(kBM, kD, 0, 1);
-      uint32_t kc = 0, vc = 0, qc = 0, pc0 = 0, pc1 = 0;
+      uint32_t kc = 0, vc = 0, qc = 0, q1c = 0, pc0 = 0, pc1 = 0;
       bool ok = true;
+      const bool split = a.q_shared_z >= 0;
       if (a.stall) ok = wait(ctl.never, 0, 31);     // injected: runs out, latches a timeout
       // Shared-memory descriptors are built once; a tile or K-step offset is
       // added to the 14-bit start-address field (addresses >> 4, all below
@@ -352,17 +380,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       // issue slots with two softmax warps.
       const uint64_t dq0 = sdesc(sQ, 16, 1024), dk0 = sdesc(sK, 16, 1024);
       const uint64_t dv0 = sdesc(sV, Tl::kBoxBytes, 1024);
-      // S_i = Q_i K^T: both K-major; step kk covers 32 bytes of each 128-byte row.
-      auto issue_qk = [&](int i, int ks) {
-        const uint64_t q = dq0 + ((uint32_t)(i * Tl::kBytes) >> 4);
+      // S_i = Q_i K^T: both K-major; step kk covers 32 bytes of each 128-byte
+      // row.  Query tile i's first box sits in buffer qb, its second (bf16)
+      // in the per-tile box after the two buffers.
+      auto issue_qk = [&](int i, int ks, int qb) {
+        const uint64_t q0 = dq0 + ((uint32_t)((2 * qb + i) * Tl::kBoxBytes) >> 4);
+        const uint64_t q1 = dq0 + ((uint32_t)((4 + i) * Tl::kBoxBytes) >> 4);
         const uint64_t k = dk0 + ((uint32_t)(ks * Tl::kBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < Tl::kSteps; ++kk) {
+          const uint32_t in_box = ((kk * 32) % 128) >> 4;
+          const uint64_t qd = (kk * 32 < 128 ? q0 : q1) + in_box;
           const uint32_t off = ((kk * 32 / 128) * Tl::kBoxBytes + (kk * 32) % 128) >> 4;
           if (F8)
-            mma_ss_f8(tmem + i * 128, q + off, k + off, idesc_qk, kk > 0);
+            mma_ss_f8(tmem + i * 128, qd, k + off, idesc_qk, kk > 0);
           else
-            mma_ss(tmem + i * 128, q + off, k + off, idesc_qk, kk > 0);
+            mma_ss(tmem + i * 128, qd, k + off, idesc_qk, kk > 0);
         }
       };
       // O_i += P_i V: P from TMEM (8 columns per step), V MN-major (kMmaK key
@@ -387,6 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         int j = 0;
         for (int s = 0; ok && s < n_slots; ++s) {
           const int nt = (cx.tokens[s] + kBN - 1) / kBN;
+          const int qb = qc & 1;                      // this slot's query buffer
+          const bool q1_new = !F8 && (!split || s == 0);
+          const bool q1_last = !F8 && (!split || s == n_slots - 1);
           for (int kt = 0; ok && kt < nt; ++kt, ++j) {
             const int ks = kc % kKSt;
             if (!(ok = wait(ctl.k_full[ks], (kc / kKSt) & 1, 11))) break;
@@ -400,11 +436,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
               ++pc0;
             }
             if (kt == 0) {
-              if (!(ok = wait(ctl.q_full, qc & 1, 14))) break;
+              if (!(ok = wait(ctl.q0_full[qb], (qc >> 1) & 1, 14))) break;
+              if (q1_new && !(ok = wait(ctl.q1_full, q1c & 1, 19))) break;
               tc_fence_after();
-              ++qc;
             }
-            issue_qk(0, ks);
+            issue_qk(0, ks, qb);
             tc_commit(smem_u32(&ctl.s_full[0]));
             if (j > 0) {
               if (!half) {
@@ -417,12 +453,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
               ++vc;
             }
             if (!half) {
-              issue_qk(1, ks);
+              issue_qk(1, ks, qb);
               tc_commit(smem_u32(&ctl.s_full[1]));
             }
             tc_commit(smem_u32(&ctl.k_empty[ks]));
             ++kc;
-            if (kt == nt - 1) tc_commit(smem_u32(&ctl.q_empty));
+            if (kt == nt - 1) {                       // the slot's last QK: its query boxes are free
+              tc_commit(smem_u32(&ctl.q0_empty[qb]));
+              ++qc;
+              if (q1_last) {
+                tc_commit(smem_u32(&ctl.q1_empty));
+                ++q1c;
+              }
+            }
           }
         }
         if (!ok) break;

@@ -281,6 +281,20 @@ class ClockSampler:
                             "max": max(r[3] for r in rows)}}
 
 
+def kernel_code_digest():
+    """sha256 of the attention kernel's device code: the text of its file
+    before the host launchers, with comments and whitespace removed (so an
+    edited comment does not retire a capture, an edited line of code does)."""
+    import hashlib
+    import re
+    src = open(os.path.join(ROOT, "bounded_kv_cache_la_b300", "csrc", "k_attn_tc.cu")).read()
+    code = src[:src.index("bool attn_tc_supported")]
+    code = re.sub(r"/\*.*?\*/", "", code, flags=re.S)
+    code = re.sub(r"//[^\n]*", "", code)
+    code = re.sub(r"\s+", "", code)
+    return hashlib.sha256(code.encode()).hexdigest()
+
+
 def kernel_traffic(sc):
     """DRAM bytes (read + write) per attention launch from the committed ncu
     summary of this workload, or None when the summary is missing or was
@@ -293,9 +307,7 @@ def kernel_traffic(sc):
     if not os.path.isfile(path):
         return None
     text = open(path).read()
-    # the kernel = the file's device code, everything before its host launchers
-    src = open(os.path.join(ROOT, "bounded_kv_cache_la_b300", "csrc", "k_attn_tc.cu")).read()
-    digest = hashlib.sha256(src[:src.index("bool attn_tc_supported")].encode()).hexdigest()
+    digest = kernel_code_digest()
     m_src = re.search(r"kernel source sha256: ([0-9a-f]{64})", text)
     m_tr = re.search(r"traffic_bytes_per_launch: (\d+)", text)
     if not m_src or not m_tr or m_src.group(1) != digest:

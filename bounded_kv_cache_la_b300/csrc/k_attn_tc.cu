@@ -9,7 +9,9 @@
 // RoPE.  Keys sit in the pool turned by their within-block position; the
 // per-slot temporal offset is moved to the query side (scores depend only on
 // position differences), so a query-rotation pass writes one rotated copy of
-// Q per slot and the attention kernel itself does no trigonometry.
+// Q per slot (for bf16 only the first half of each row, which holds every
+// temporal pair, plus one shared copy of the second half) and the attention
+// kernel itself does no trigonometry.
 //
 // Gather.  K/V tiles are TMA-loaded straight from the slot's pool page (the
 // slot table says which page), 128 keys x 64 dims per box, 128-byte swizzle;
@@ -35,7 +37,9 @@
 //
 // Softmax.  Base-2 online softmax with a lazy rescale: the running max moves
 // only when a row's max grows by more than 8 (a factor 256), then O and l are
-// rescaled.  The row max is a tree of 3-input maxes; scale-and-subtract and
+// rescaled.  The row max is only taken on a unit's first key tile or when a
+// row's tile sum exceeds 2^8 (below that no value can pass the bound); it is
+// a tree of 3-input maxes.  Scale-and-subtract and
 // the row sum use packed fp32x2 arithmetic.  The exponentials are split
 // between the MUFU unit (ex2.approx) and the FMA pipe as a build option:
 // kEmuPairs of every 16 column pairs use 2^x = 2^n * p(x - n), n = rint(x) (Cody and Waite's

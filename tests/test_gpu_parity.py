@@ -114,11 +114,22 @@ def test_external_history_retrieval_at_10000_blocks():
 def test_convkv_memory_and_attention():
     """ConvKV at reduced size: memory rings equal the oracle's FIFO of
     compressed tokens; attention over memory + window + current."""
-    import torch
     sc = C4_CONVKV.with_(num_heads=4, grid_h=5, grid_w=9, mem_slots=240)
-    T = sc.tokens_per_block                           # 135 tokens -> 27 per eviction
-    n = 16
-    keep = {0, 3, 4, 8, 12, 15}
+    _convkv_case(sc, 16, {0, 3, 4, 8, 12, 15})        # 135 tokens -> 27 per eviction
+
+
+@pytest.mark.parametrize("kernel,stride", [(3, 2), (4, 4), (7, 5)])
+def test_convkv_other_kernel_sizes(kernel, stride):
+    """Kernel sizes other than 5 (the per-tap weight path), windows that
+    overlap (3/2), tile (4/4) or reach past the stride (7/5), and evictions
+    that do not divide the block evenly."""
+    sc = C4_CONVKV.with_(num_heads=3, grid_h=5, grid_w=9, mem_slots=200, conv_kernel=kernel,
+                         conv_stride=stride)
+    _convkv_case(sc, 12, {4, 8, 11})
+
+
+def _convkv_case(sc, n, keep):
+    import torch
     cache, ctxs, outs = H.run_stream(sc, n, keep, n_steps=2)
     vals = H.Values(sc)
     w = gen.conv_weights_np(sc, 0)

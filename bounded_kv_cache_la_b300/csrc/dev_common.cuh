@@ -43,11 +43,6 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float(((uint32_t)b) << 16);
 }
 
-__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
-  __nv_bfloat16 h = __float2bfloat16_rn(x);
-  return *reinterpret_cast<uint16_t*>(&h);
-}
-
 // Two fp32 -> bf16 (round to nearest even) in one instruction; lo in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;

@@ -33,6 +33,7 @@ EXPORTS = (
     "la_debug_inject",
 )
 LA_INJECT_ATTN_STALL = 1
+LA_INJECT_BAD_FRAME = 2
 
 
 class la_cache_config(ctypes.Structure):

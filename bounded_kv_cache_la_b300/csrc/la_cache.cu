@@ -61,6 +61,8 @@ struct la_cache {
   int num_sms = 148;
   std::vector<cudaEvent_t> prof_start, prof_stop;
   int inject_stall = 0;             // tensor-core launches still to stall (tests)
+  int inject_bad_frame = 0;         // attention launches still to get a bad slot table (tests)
+  DevContext dctx_inject{};         // host copy of that table (the upload reads it)
   size_t prof_next = 0;
 };
 
@@ -168,6 +170,7 @@ void compute_layout(const la_cache_config& c, Layout& L) {
   L.err = take(sizeof(DevError));
   L.ctx = take(sizeof(DevContext));
   L.ctx_final = take(sizeof(DevContext));
+  L.ctx_inject = take(sizeof(DevContext));
   L.topk = take(sizeof(DevTopk));
   // e4m3 amax scratch, one [2][H] slice per frame plus one for the current
   // pages, so page writes to different frames may run on different streams
@@ -837,6 +840,18 @@ la_status chunk_attention(la_cache* c, int layer, const void* q, const void* k_c
   }
   const DevContext* dctx =
       reinterpret_cast<const DevContext*>(c->pool + (final ? c->L.ctx_final : c->L.ctx));
+  if (c->inject_bad_frame > 0) {
+    // failure injection: the first slot names a frame past the pool's frames
+    --c->inject_bad_frame;
+    c->dctx_inject = final ? c->dctx_final : c->dctx;
+    c->dctx_inject.kind[0] = SLOT_FRAME;
+    c->dctx_inject.frame[0] = c->L.n_frames + 7;
+    st = cuda_status(c, cudaMemcpyAsync(c->pool + c->L.ctx_inject, &c->dctx_inject, sizeof(DevContext),
+                                        cudaMemcpyHostToDevice, s),
+                     "upload injected slot table");
+    if (st != LA_OK) return st;
+    dctx = reinterpret_cast<const DevContext*>(c->pool + c->L.ctx_inject);
+  }
   DevError* err = reinterpret_cast<DevError*>(c->pool + c->L.err);
   if (c->tc) {
     QrotArgs qa{};
@@ -1104,6 +1119,10 @@ uint64_t la_launch_count(void) { return la::g_launches.load(std::memory_order_re
 
 la_status la_debug_inject(la_cache_t* c, int what, int count) {
   if (!c || count < 0) return LA_ERR_INVALID_ARG;
+  if (what == LA_INJECT_BAD_FRAME) {
+    c->inject_bad_frame = count;
+    return LA_OK;
+  }
   if (what != LA_INJECT_ATTN_STALL) return LA_ERR_INVALID_ARG;
   if (!c->tc) return LA_ERR_UNSUPPORTED;
   c->inject_stall = count;

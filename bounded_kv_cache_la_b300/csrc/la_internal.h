@@ -65,6 +65,7 @@ struct Layout {
   size_t cur_pages;                // 2 pages: current block K', V
   size_t qrot;                     // [S][H][T][D] rotated queries (tensor path), kv dtype
   size_t rope_t2;                  // bf16 tensor path: temporal table as (cos, cos, sin, sin)
+  size_t ctx_inject;               // slot table of an injected failure (la_debug_inject)
   size_t qscale;                   // e4m3 tensor path: [H][T] fp32 query scales
   size_t mem;                      // ConvKV [L][3][H][cap][D] bf16 (raw K, V, rotated K)
   size_t total;

@@ -262,6 +262,12 @@ la_status la_set_profile_events(la_cache_t* cache, void* const* starts, void* co
  * stays usable.  LA_ERR_UNSUPPORTED when the cache runs the CUDA-core
  * kernel. */
 #define LA_INJECT_ATTN_STALL 1
+/* LA_INJECT_BAD_FRAME: the next `count` attention launches of this cache (either
+ * kernel) read a slot table whose first slot names a frame past the end of the
+ * pool.  The kernel's bounds check rejects the table before any load, latches
+ * LA_ERR_DEVICE in the error word (the message names the kernel) and returns;
+ * the CUDA context stays usable. */
+#define LA_INJECT_BAD_FRAME 2
 la_status la_debug_inject(la_cache_t* cache, int what, int count);
 
 /* Number of kernels this library has enqueued since it was loaded. */

@@ -30,7 +30,7 @@ EXPORTS = (
     "la_cache_load_history", "la_fill_window", "la_get_error", "la_context_plan",
     "la_debug_page", "la_debug_memory", "la_set_profile_events", "la_launch_count",
     "la_status_string", "la_pose_topk_noalloc", "la_refresh_sink", "la_prefetch_context",
-    "la_debug_inject",
+    "la_debug_inject", "la_cache_state_bytes", "la_cache_save_state", "la_cache_restore",
 )
 LA_INJECT_ATTN_STALL = 1
 LA_INJECT_BAD_FRAME = 2
@@ -108,6 +108,9 @@ def load() -> ctypes.CDLL:
         "la_cache_required_bytes": (sz, [cfgp]),
         "la_cache_create": (i32, [cfgp, vp, sz, vp, vp, ctypes.POINTER(vp)]),
         "la_cache_destroy": (i32, [vp]),
+        "la_cache_state_bytes": (sz, [vp]),
+        "la_cache_save_state": (i32, [vp, vp, sz]),
+        "la_cache_restore": (i32, [cfgp, vp, sz, vp, vp, sz, vp, ctypes.POINTER(vp)]),
         "la_select_context": (i32, [vp, ctypes.POINTER(ctypes.c_float), ctxp, vp]),
         "la_fill_block": (i32, [vp, i32, i32, vp, vp, vp]),
         "la_chunk_attention": (i32, [vp, i32, vp, vp, vp, vp, vp]),
@@ -230,23 +233,48 @@ class Cache:
 
     Methods map one-to-one onto the C calls; tensors are passed by address."""
 
-    def __init__(self, cfg: la_cache_config, conv_w=None, stream=None):
+    def __init__(self, cfg: la_cache_config, conv_w=None, stream=None, restore=None):
+        """restore: (pool_bytes, state) from save_checkpoint() to resume a
+        stream instead of starting one."""
         import torch
         self.lib = load()
         self.cfg = cfg
         nbytes = la_cache_required_bytes(cfg)
         if nbytes == 0:
             raise LaError(LA_ERR_INVALID_ARG, "la_cache_required_bytes")
+        self.nbytes = nbytes
         self.pool = torch.empty(nbytes + 256, dtype=torch.uint8, device="cuda")
         base = self.pool.data_ptr()
         self.base = (base + 255) // 256 * 256
         self.conv_w = conv_w
         h = ctypes.c_void_p()
-        _check(self.lib.la_cache_create(ctypes.byref(cfg), ctypes.c_void_p(self.base), nbytes,
-                                        _ptr(conv_w) if conv_w is not None else None,
-                                        _stream_handle(stream), ctypes.byref(h)),
-               "la_cache_create")
+        cw = _ptr(conv_w) if conv_w is not None else None
+        if restore is None:
+            _check(self.lib.la_cache_create(ctypes.byref(cfg), ctypes.c_void_p(self.base), nbytes, cw,
+                                            _stream_handle(stream), ctypes.byref(h)),
+                   "la_cache_create")
+        else:
+            pool_bytes, state = restore
+            self.pool_view().copy_(pool_bytes)
+            buf = ctypes.create_string_buffer(bytes(state), len(state))
+            _check(self.lib.la_cache_restore(ctypes.byref(cfg), ctypes.c_void_p(self.base), nbytes, cw,
+                                             buf, len(state), _stream_handle(stream), ctypes.byref(h)),
+                   "la_cache_restore")
         self.h = h
+
+    def pool_view(self):
+        """The pool's la_cache_required_bytes bytes as a uint8 tensor."""
+        off = self.base - self.pool.data_ptr()
+        return self.pool[off:off + self.nbytes]
+
+    def save_checkpoint(self):
+        """(pool bytes on the CPU, host-state blob) between blocks."""
+        import torch
+        n = self.lib.la_cache_state_bytes(self.h)
+        buf = ctypes.create_string_buffer(n)
+        _check(self.lib.la_cache_save_state(self.h, buf, n), "la_cache_save_state")
+        torch.cuda.synchronize()
+        return self.pool_view().cpu(), buf.raw
 
     def close(self):
         if getattr(self, "h", None):

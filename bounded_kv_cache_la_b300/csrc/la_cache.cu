@@ -45,7 +45,7 @@ struct la_cache {
   DevContext dctx{}, dctx_final{};
   std::vector<int> frame_of;        // block -> frame (-1 none)
   std::vector<int> free_frames;
-  std::deque<int> window;
+  std::deque<int> window;           // exact window blocks, oldest first
   std::vector<int> dyn;
   std::vector<int> pre;             // dynamic sink fetched ahead for block pre_for
   int pre_for = -1;
@@ -393,6 +393,66 @@ la_status check_usable(la_cache* c) {
 
 }  // namespace
 
+// ------------------------------------------------------------ checkpoint
+// Host-state blob: magic, version, the config, then the block counter,
+// fetch-ahead block, ConvKV ring position, the last query pose, and the
+// frame table, free frames, dynamic sink, fetched-ahead picks and the
+// per-frame / per-layer flags (each vector as a count and its elements).
+namespace {
+constexpr uint32_t kStateMagic = 0x5343414cu;   // "LACS"
+constexpr uint32_t kStateVersion = 1;
+
+struct Writer {
+  std::vector<char> buf;
+  template <class T> void put(const T& x) {
+    const char* p = reinterpret_cast<const char*>(&x);
+    buf.insert(buf.end(), p, p + sizeof(T));
+  }
+  template <class T> void put_vec(const std::vector<T>& v) {
+    put<int64_t>((int64_t)v.size());
+    for (const T& x : v) put(x);
+  }
+};
+struct Reader {
+  const char* p;
+  size_t left;
+  bool ok = true;
+  template <class T> T get() {
+    T x{};
+    if (left < sizeof(T)) { ok = false; return x; }
+    std::memcpy(&x, p, sizeof(T));
+    p += sizeof(T);
+    left -= sizeof(T);
+    return x;
+  }
+  template <class T> std::vector<T> get_vec(int64_t max_n) {
+    const int64_t n = get<int64_t>();
+    std::vector<T> v;
+    if (!ok || n < 0 || n > max_n) { ok = false; return v; }
+    v.resize((size_t)n);
+    for (auto& x : v) x = get<T>();
+    return v;
+  }
+};
+
+void write_state(const la_cache* c, Writer& w) {
+  w.put(kStateMagic);
+  w.put(kStateVersion);
+  w.put(c->cfg);
+  w.put<int32_t>(c->b);
+  w.put<int32_t>(c->pre_for);
+  w.put<int32_t>(c->mem_n);
+  w.put<int32_t>(c->mem_head);
+  for (float x : c->query_kp) w.put(x);
+  w.put_vec(c->frame_of);
+  w.put_vec(c->free_frames);
+  w.put_vec(c->dyn);
+  w.put_vec(c->pre);
+  w.put_vec(std::vector<int>(c->window.begin(), c->window.end()));
+  for (const auto& f : c->filled) w.put_vec(f);
+}
+}  // namespace
+
 extern "C" {
 
 const char* la_status_string(la_status s) {
@@ -444,9 +504,11 @@ la_status la_context_plan(const la_cache_config* cfg, int block, const int32_t* 
   return LA_OK;
 }
 
-la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t pool_bytes,
-                          const void* conv_w, void* stream, la_cache_t** out) {
-  Range nvtx_range("la_cache_create");
+// Builds the cache object over the caller's pool; init_pool: zero the
+// control and ring regions and build the RoPE tables (a restored pool
+// already holds them).
+static la_status create_cache(const la_cache_config* cfg, void* dev_pool, size_t pool_bytes,
+                              const void* conv_w, void* stream, bool init_pool, la_cache_t** out) {
   if (!out) return LA_ERR_INVALID_ARG;
   *out = nullptr;
   la_status st = validate(cfg);
@@ -492,8 +554,8 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
   int dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
-  st = cuda_status(c, cudaMemsetAsync(c->pool, 0, L.pose_tab, s), "pool init");
-  if (st == LA_OK)
+  if (init_pool) st = cuda_status(c, cudaMemsetAsync(c->pool, 0, L.pose_tab, s), "pool init");
+  if (st == LA_OK && init_pool)
     st = cuda_status(c,
                      launch_init_tables(reinterpret_cast<float2*>(c->pool + L.rope_t), L.max_t,
                                         cfg->rope_t, reinterpret_cast<float2*>(c->pool + L.rope_h),
@@ -502,12 +564,12 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
                                         cfg->rope_w, (double)cfg->rope_theta,
                                         const_cast<float4*>(c->rope.tab_t2), s),
                      "rope tables");
-  if (st == LA_OK && cfg->kv_dtype == LA_E4M3)
+  if (st == LA_OK && init_pool && cfg->kv_dtype == LA_E4M3)
     st = cuda_status(c, cudaMemsetAsync(c->pool + L.scales, 0, L.frames - L.scales, s),
                      "scale init");
   // ConvKV rings start zeroed: attention reads whole tiles, so ring rows
   // past the valid count must hold finite values (they get weight 0).
-  if (st == LA_OK && !is_prsink(*cfg))
+  if (st == LA_OK && init_pool && !is_prsink(*cfg))
     st = cuda_status(c, cudaMemsetAsync(c->pool + L.mem, 0, L.total - L.mem, s), "memory init");
   c->tc = tc_eligible(*cfg, L);
   if (st == LA_OK && c->tc) {
@@ -537,6 +599,86 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
     delete c;
     return st;
   }
+  *out = c;
+  return LA_OK;
+}
+
+la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t pool_bytes,
+                          const void* conv_w, void* stream, la_cache_t** out) {
+  Range nvtx_range("la_cache_create");
+  return create_cache(cfg, dev_pool, pool_bytes, conv_w, stream, true, out);
+}
+
+
+size_t la_cache_state_bytes(la_cache_t* c) {
+  if (!c) return 0;
+  Writer w;
+  write_state(c, w);
+  return w.buf.size();
+}
+
+la_status la_cache_save_state(la_cache_t* c, void* host_buf, size_t cap) {
+  la_status st = check_usable(c);
+  if (st != LA_OK) return st;
+  if (!host_buf) return LA_ERR_INVALID_ARG;
+  if (c->selected) return LA_ERR_STATE;           // only between blocks
+  Writer w;
+  write_state(c, w);
+  if (cap < w.buf.size()) return LA_ERR_INVALID_ARG;
+  std::memcpy(host_buf, w.buf.data(), w.buf.size());
+  return LA_OK;
+}
+
+la_status la_cache_restore(const la_cache_config* cfg, void* dev_pool, size_t pool_bytes,
+                           const void* conv_w, const void* state, size_t state_bytes, void* stream,
+                           la_cache_t** out) {
+  Range nvtx_range("la_cache_restore");
+  if (!out) return LA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !state) return LA_ERR_INVALID_ARG;
+  Reader r{static_cast<const char*>(state), state_bytes};
+  const uint32_t magic = r.get<uint32_t>(), version = r.get<uint32_t>();
+  const la_cache_config saved = r.get<la_cache_config>();
+  if (!r.ok || magic != kStateMagic || version != kStateVersion ||
+      std::memcmp(&saved, cfg, sizeof(saved)) != 0)
+    return LA_ERR_INVALID_ARG;
+  la_cache_t* c = nullptr;
+  la_status st = create_cache(cfg, dev_pool, pool_bytes, conv_w, stream, false, &c);
+  if (st != LA_OK) return st;
+  const int32_t b = r.get<int32_t>(), pre_for = r.get<int32_t>();
+  const int32_t mem_n = r.get<int32_t>(), mem_head = r.get<int32_t>();
+  float kp[34];
+  for (float& x : kp) x = r.get<float>();
+  const int64_t max_ids = std::max<int64_t>(c->frame_of.size(), (int64_t)b * 2 + 2);
+  auto frame_of = r.get_vec<int>(max_ids);
+  auto free_frames = r.get_vec<int>(c->L.n_frames);
+  auto dyn = r.get_vec<int>(LA_MAX_TOPK);
+  auto pre = r.get_vec<int>(LA_MAX_TOPK);
+  auto window = r.get_vec<int>(cfg->window);
+  std::vector<std::vector<char>> filled(c->L.n_frames);
+  for (auto& f : filled) {
+    f = r.get_vec<char>(cfg->num_layers);
+    if ((int)f.size() != cfg->num_layers) r.ok = false;
+  }
+  bool ok = r.ok && r.left == 0 && b >= 0 && mem_n >= 0 && mem_n <= cfg->mem_slots && mem_head >= 0 &&
+            mem_head < std::max(cfg->mem_slots, 1) && (int64_t)frame_of.size() >= (int64_t)c->frame_of.size();
+  for (int f : frame_of) ok = ok && f >= -1 && f < c->L.n_frames;
+  for (int f : free_frames) ok = ok && f >= 0 && f < c->L.n_frames;
+  if (!ok) {
+    delete c;
+    return LA_ERR_INVALID_ARG;
+  }
+  c->b = b;
+  c->pre_for = pre_for;
+  c->mem_n = mem_n;
+  c->mem_head = mem_head;
+  std::memcpy(c->query_kp, kp, sizeof(kp));
+  c->frame_of = std::move(frame_of);
+  c->free_frames = std::move(free_frames);
+  c->dyn = std::move(dyn);
+  c->pre = std::move(pre);
+  c->window.assign(window.begin(), window.end());
+  c->filled = std::move(filled);
   *out = c;
   return LA_OK;
 }

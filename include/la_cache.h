@@ -124,6 +124,27 @@ la_status la_cache_create(const la_cache_config* cfg, void* dev_pool, size_t poo
  * work enqueued for this cache has completed.  The pool stays the caller's. */
 la_status la_cache_destroy(la_cache_t* cache);
 
+/* Checkpoint and resume of a stream between blocks (the pages describe no
+ * such facility; it serves callers that restart a long stream).  The device
+ * state is the pool, which the caller owns and copies; the host state -- the
+ * block counter, the frame table and free frames, the window, the dynamic
+ * sink and any picks fetched ahead, the ConvKV ring position -- goes into a
+ * host buffer of la_cache_state_bytes(cache) bytes:
+ *   la_cache_save_state: only between blocks (after the append of a block's
+ *     last layer, before the next select; LA_ERR_STATE otherwise);
+ *     LA_ERR_INVALID_ARG when `cap` is too small.  The pool bytes must be
+ *     copied after the cache's enqueued work has completed.
+ *   la_cache_restore: builds a cache over a pool that holds the saved pool
+ *     bytes (at any device address; same size rule as la_cache_create) and
+ *     continues the stream at the saved block.  The blob carries the config:
+ *     a different config or a malformed blob gives LA_ERR_INVALID_ARG.
+ *     The pool is not initialised.  `conv_w` as for la_cache_create. */
+size_t la_cache_state_bytes(la_cache_t* cache);
+la_status la_cache_save_state(la_cache_t* cache, void* host_buf, size_t cap);
+la_status la_cache_restore(const la_cache_config* cfg, void* dev_pool, size_t pool_bytes,
+                           const void* conv_w, const void* state, size_t state_bytes,
+                           void* stream, la_cache_t** out);
+
 /* Starts block b (b = number of blocks appended so far).  Runs the pose
  * retrieval kernel on `stream` ([LA] 方法, Dynamic Sink): the centred 34-value
  * descriptor of `query_pose` (host, 17 (x, y) keypoints) is scored by cosine

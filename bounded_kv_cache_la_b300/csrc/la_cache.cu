@@ -664,6 +664,9 @@ la_status la_cache_restore(const la_cache_config* cfg, void* dev_pool, size_t po
             mem_head < std::max(cfg->mem_slots, 1) && (int64_t)frame_of.size() >= (int64_t)c->frame_of.size();
   for (int f : frame_of) ok = ok && f >= -1 && f < c->L.n_frames;
   for (int f : free_frames) ok = ok && f >= 0 && f < c->L.n_frames;
+  // block ids index the frame table
+  for (const auto* ids : {&dyn, &pre, &window})
+    for (int id : *ids) ok = ok && id >= 0 && id < (int64_t)frame_of.size();
   if (!ok) {
     delete c;
     return LA_ERR_INVALID_ARG;

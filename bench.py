@@ -131,7 +131,7 @@ class OracleSample:
     heads x n_rows query rows against the full 32760-key context.  Inputs are
     generated once (not timed); run() times the oracle's computation."""
 
-    def __init__(self, sc, n_heads=8, n_rows=512):
+    def __init__(self, sc, n_heads=8, n_rows=2048):
         from oracle import stream as ostream
         from synth import gen
         self.sc = sc
@@ -194,7 +194,7 @@ def cpu_baseline():
     BLAS thread, and (in a child process whose BLAS is limited to one thread
     before NumPy loads) a smaller sample on one thread."""
     smp = OracleSample(workload())
-    dt = min(smp.run() for _ in range(2))
+    dt = min(smp.run() for _ in range(3))          # ~10 s of CPU work on 16 cores
     out = {"value": smp.flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
            "kind": "oracle", "sample": smp.text, "seconds": dt}
     try:

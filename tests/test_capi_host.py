@@ -99,3 +99,26 @@ def test_plan_rejects_bad_dynamic_ids():
     for ids in ([0], [9], [3, 3], [50]):
         with pytest.raises(capi.LaError):
             capi.la_context_plan(cfg, 10, ids)
+
+
+def test_restore_rejects_foreign_blobs(lib):
+    """la_cache_restore checks the blob before it touches the device: a blob
+    that is not a state blob, or that carries another config, is refused."""
+    import ctypes
+    cfg = capi.config_for(C2_MID)
+    other = capi.config_for(C2_MID.with_(dyn_topk=2))
+    out = ctypes.c_void_p()
+    fake_pool = ctypes.c_void_p(0x10000)       # never dereferenced on these paths
+
+    def restore(blob, c=cfg):
+        buf = ctypes.create_string_buffer(blob, len(blob))
+        return lib.la_cache_restore(ctypes.byref(c), fake_pool, 1 << 30, None, buf, len(blob), None,
+                                    ctypes.byref(out))
+
+    header = (0x5343414C).to_bytes(4, "little") + (1).to_bytes(4, "little")
+    assert restore(b"not a cache state blob") == capi.LA_ERR_INVALID_ARG
+    assert restore(header) == capi.LA_ERR_INVALID_ARG                       # truncated
+    assert restore(header + bytes(other)) == capi.LA_ERR_INVALID_ARG        # another config
+    wrong_version = (0x5343414C).to_bytes(4, "little") + (2).to_bytes(4, "little")
+    assert restore(wrong_version + bytes(cfg)) == capi.LA_ERR_INVALID_ARG
+    assert lib.la_cache_state_bytes(None) == 0

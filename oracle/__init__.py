@@ -23,7 +23,9 @@ function that takes it.
 
 Parity status of each function (what pins it in tests/test_oracle_*.py):
   pose.descriptor / pose.cosine_scores / pose.select_topk : pinned
-  rope.*                 : pinned (norm, identity, shift, closed form, golden)
+  rope.*                 : pinned (complex multiplication for the default and
+                           explicit (t, h, w) splits, norm, identity, shift,
+                           closed form, golden)
   attention.softmax_attention : pinned (torch SDPA / scipy softmax, uniform V)
   stream.*               : pinned (constant KV length, window/sink invariants)
   convkv.*               : pinned (torch conv1d, closed-form weights, FIFO cap)

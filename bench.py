@@ -906,8 +906,9 @@ def run_ours(a):
                          "max": float(np.max(block_ms))},
             "frac_of_bf16_peak": value / pk["bf16_tflops"],
             "frac_of_bf16_peak_sustained": value / peak_sus,
-            "attn_call_ms": {"mean": float(attn_ms.mean()), "min": float(attn_ms.min()),
-                             "max": float(attn_ms.max()), "n": int(attn_ms.size)},
+            "attn_call_ms": {"mean": float(attn_ms.mean()), "median": float(np.median(attn_ms)),
+                             "min": float(attn_ms.min()), "max": float(attn_ms.max()),
+                             "n": int(attn_ms.size)},
             "fills_per_block": fills_timed / a.steps,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_sus,
                          "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": traffic,

@@ -82,8 +82,28 @@ def test_plan_matches_oracle_prsink(sc, n):
         assert got["mem_tokens"] == 0
 
 
-def test_plan_matches_oracle_convkv():
-    sc = C4_CONVKV
+@pytest.mark.parametrize("sc", [
+    C2_MID.with_(dyn_topk=8, window=6),                       # 16 slots
+    C2_MID.with_(static_sink=0),
+    C2_MID.with_(dyn_topk=0),
+    C2_MID.with_(static_sink=0, dyn_topk=0, window=1),
+    C5_FP8.with_(window=5, dyn_topk=6),
+])
+def test_plan_matches_oracle_other_policies(sc):
+    """Slot order, RoPE bases and KV length for other sink / top-k / window
+    settings, over a stream long enough to fill every slot."""
+    n = 40
+    cfg = capi.config_for(sc, max_history=n + 2)
+    for ctx in stream.plan_stream(sc, gen.poses(sc, n_blocks=n), n):
+        got = capi.la_context_plan(cfg, ctx.block, ctx.dyn_ids)
+        assert got["blocks"] == ctx.blocks
+        assert got["t0"] == ctx.t0
+        assert got["kv_len"] == ctx.kv_len
+
+
+@pytest.mark.parametrize("kernel,stride", [(5, 5), (3, 2), (4, 4), (7, 5)])
+def test_plan_matches_oracle_convkv(kernel, stride):
+    sc = C4_CONVKV.with_(conv_kernel=kernel, conv_stride=stride)
     cfg = capi.config_for(sc)
     for b in range(0, 1000, 7):
         ctx = stream.plan_convkv(sc, b)

@@ -142,3 +142,35 @@ def test_restore_rejects_foreign_blobs(lib):
     wrong_version = (0x5343414C).to_bytes(4, "little") + (2).to_bytes(4, "little")
     assert restore(wrong_version + bytes(cfg)) == capi.LA_ERR_INVALID_ARG
     assert lib.la_cache_state_bytes(None) == 0
+
+
+def test_struct_layouts_match_header(tmp_path):
+    """The ctypes mirrors of la_cache_config and la_context have the size and
+    field offsets the C compiler gives the header's structs, and the
+    header's constants match the binding's."""
+    import ctypes
+    fields = {"la_cache_config": [f[0] for f in capi.la_cache_config._fields_],
+              "la_context": [f[0] for f in capi.la_context._fields_]}
+    lines = ['#include <stdio.h>', '#include "la_cache.h"', "int main(void) {"]
+    for st, names in fields.items():
+        lines.append(f'  printf("{st} %zu\\n", sizeof({st}));')
+        for n in names:
+            lines.append(f'  printf("{st}.{n} %zu\\n", offsetof({st}, {n}));')
+    for c in ("LA_MAX_SLOTS", "LA_MAX_TOPK", "LA_INJECT_ATTN_STALL", "LA_INJECT_BAD_FRAME",
+              "LA_ERR_DEVICE", "LA_ATTN_SIMT", "LA_HISTORY_EXTERNAL"):
+        lines.append(f'  printf("{c} %d\\n", (int){c});')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    for st, names in fields.items():
+        cls = getattr(capi, st)
+        assert int(got[st]) == ctypes.sizeof(cls), st
+        for n in names:
+            assert int(got[f"{st}.{n}"]) == getattr(cls, n).offset, (st, n)
+    for c in ("LA_MAX_SLOTS", "LA_MAX_TOPK", "LA_INJECT_ATTN_STALL", "LA_INJECT_BAD_FRAME",
+              "LA_ERR_DEVICE", "LA_ATTN_SIMT", "LA_HISTORY_EXTERNAL"):
+        assert int(got[c]) == getattr(capi, c), c

@@ -174,3 +174,40 @@ def test_struct_layouts_match_header(tmp_path):
     for c in ("LA_MAX_SLOTS", "LA_MAX_TOPK", "LA_INJECT_ATTN_STALL", "LA_INJECT_BAD_FRAME",
               "LA_ERR_DEVICE", "LA_ATTN_SIMT", "LA_HISTORY_EXTERNAL"):
         assert int(got[c]) == getattr(capi, c), c
+
+
+def test_fast_division_magic(tmp_path):
+    """The kernels divide token indices by run-time constants with a
+    multiply-high, an add and a shift (FastDiv in csrc/la_internal.h).  The
+    host-made multipliers, used the way the device uses them, give n / d
+    exactly for every divisor up to 5000 on 4000 spread numerators each and
+    on the edge numerators (0, d - 1, d, 2^31 - 1)."""
+    src = tmp_path / "fastdiv.cpp"
+    src.write_text(r'''
+#include <cstdio>
+#include "la_internal.h"
+int main() {
+  long long bad = 0, checked = 0;
+  auto check = [&](const la::FastDiv& f, uint32_t n, uint32_t d) {
+    const uint32_t q = (uint32_t)((((uint64_t)n * f.m >> 32) + n) >> f.l);   // umulhi + add + shift
+    bad += q != n / d;
+    ++checked;
+  };
+  for (uint32_t d = 1; d <= 5000; ++d) {
+    const la::FastDiv f = la::make_fastdiv(d);
+    for (uint32_t k = 0; k < 4000; ++k)
+      check(f, (uint32_t)(((uint64_t)k * 2654435761u + d * 40503u) % (1u << 31)), d);
+    for (uint32_t n : {0u, d - 1, d, 0x7fffffffu}) check(f, n, d);
+  }
+  std::printf("%lld %lld\n", checked, bad);
+  return bad != 0;
+}
+''')
+    exe = tmp_path / "fastdiv"
+    subprocess.run(["g++", "-std=c++17", "-I", os.path.join(ROOT, "include"),
+                    "-I", os.path.join(ROOT, "bounded_kv_cache_la_b300", "csrc"),
+                    "-I", os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include"),
+                    str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    checked, bad = map(int, out.stdout.split())
+    assert out.returncode == 0 and bad == 0 and checked == 5000 * 4004

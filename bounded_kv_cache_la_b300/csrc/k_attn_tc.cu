@@ -40,13 +40,9 @@
 // rescaled.  The row max is only taken on a unit's first key tile or when a
 // row's tile sum exceeds 2^8 (below that no value can pass the bound); it is
 // a tree of 3-input maxes.  Scale-and-subtract and
-// the row sum use packed fp32x2 arithmetic.  The exponentials are split
-// between the MUFU unit (ex2.approx) and the FMA pipe as a build option:
-// kEmuPairs of every 16 column pairs use 2^x = 2^n * p(x - n), n = rint(x) (Cody and Waite's
-// reduction, exact in base 2), p a degree-3 minimax polynomial for 2^f on
-// [-1/2, 1/2] (max relative error 7.5e-5, fitted by csrc/fit_exp2_poly.py),
-// and 2^n added to the exponent bits.  P is rounded to bf16 (relative error
-// 2^-9) before the PV product either way.
+// the row sum use packed fp32x2 arithmetic; the exponentials run on the MUFU
+// unit (ex2.approx).  P is rounded to bf16 (relative error 2^-9) before the
+// PV product.
 //
 // Every wait is bounded (2 s, or the injected limit); on timeout the kernel
 // latches LA_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM
@@ -99,18 +95,6 @@ struct Tile {
   static_assert(kSmem <= 227 * 1024, "over the per-block shared memory limit");
 };
 constexpr float kRescaleThreshold = 8.0f;                 // log2(256)
-// Measured at the 14B shape (one call, B300): 0 -> 2.75 ms, 4 -> 2.91,
-// 6 -> 2.98, 8 -> 3.08: the exponentials are not the binding unit here, so
-// the default keeps them all on MUFU.
-#ifndef LA_EMU_PAIRS
-#define LA_EMU_PAIRS 0
-#endif
-constexpr int kEmuPairs = LA_EMU_PAIRS;                   // of every 16 column pairs
-static_assert(kEmuPairs >= 0 && kEmuPairs <= 16, "kEmuPairs out of range");
-
-// 2^f on [-1/2, 1/2]: c0 + c1 f + c2 f^2 + c3 f^3 (fp32 bit patterns).
-constexpr uint32_t kP0 = 0x3f7ffb49u, kP1 = 0x3f31798du, kP2 = 0x3e786f0du, kP3 = 0x3d61fbb0u;
-constexpr float kRoundMagic = 12582912.0f;                // 1.5 * 2^23
 
 struct Ctl {
   uint64_t q0_full[2], q0_empty[2];   // slot-dependent query boxes, per buffer
@@ -190,24 +174,6 @@ __device__ __forceinline__ const CUtensorMap* kv_map(const TcAttnArgs& a, const 
   }
   row = a.mem_row0 + (which == 0 ? 2 : 1) * a.H + h;     // rotated-key ring / value ring
   return &a.tm_mem;
-}
-
-// 2^x for a pair on the FMA pipe (x <= 2^7; x below -125 gives 2^-125-ish,
-// negligible next to the row max's 1).
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  x.x = fmaxf(x.x, -125.f);
-  x.y = fmaxf(x.y, -125.f);
-  const float2 t = fadd2(x, make_float2(kRoundMagic, kRoundMagic));      // rint(x) in the low bits
-  const float2 n = fsub2(t, make_float2(kRoundMagic, kRoundMagic));
-  const float2 f = fsub2(x, n);                                          // exact, |f| <= 1/2
-  const float2 c3 = make_float2(__uint_as_float(kP3), __uint_as_float(kP3));
-  const float2 c2 = make_float2(__uint_as_float(kP2), __uint_as_float(kP2));
-  const float2 c1 = make_float2(__uint_as_float(kP1), __uint_as_float(kP1));
-  const float2 c0 = make_float2(__uint_as_float(kP0), __uint_as_float(kP0));
-  float2 p = ffma2(ffma2(ffma2(c3, f, c2), f, c1), f, c0);
-  p.x = __int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23));
-  p.y = __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23));
-  return p;
 }
 
 // Scales of slot s for head h (e4m3 cache): key scale (which = 0) or value
@@ -566,12 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             for (int e = 0; e < kBN / 2; ++e) {
               const float2 x = ffma2(make_float2(sv[2 * e], sv[2 * e + 1]), c2, nm2);
               float2 p;
-              if (!F8 && (e & 15) < kEmuPairs) {
-                p = exp2_poly2(x);
-              } else {
-                p.x = ex2(x.x);
-                p.y = ex2(x.y);
-              }
+              p.x = ex2(x.x);
+              p.y = ex2(x.y);
               sv[2 * e] = p.x;
               sv[2 * e + 1] = p.y;
               acc[e & 3] = fadd2(acc[e & 3], p);

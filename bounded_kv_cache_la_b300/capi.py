@@ -132,7 +132,7 @@ def load() -> ctypes.CDLL:
         "la_launch_count": (ctypes.c_uint64, []),
         "la_status_string": (ctypes.c_char_p, [i32]),
         "la_pose_topk_noalloc": (i32, [vp, vp, i32, ctypes.POINTER(ctypes.c_float), i32, i32, i32,
-                                       i32, vp, vp, vp, vp]),
+                                       i32, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -202,18 +202,19 @@ def la_context_plan(cfg: la_cache_config, block: int, dyn_ids=()) -> dict:
 
 
 def la_pose_topk_noalloc(table, inv_norm, query_kp, pose_row, c0, c1, k, ids_out, scores_out,
-                         n_out, stream=None):
+                         n_out, status_out, stream=None):
     """Pose top-k with the library's fixed scratch (no device allocation).
 
     table [max_rows, 36] and inv_norm [max_rows] are caller-owned float32
-    device tensors; ids_out (int32), scores_out (float32) hold k + 1 entries
-    and n_out (int32) one, all on the device.  query_kp: host, 17 x 2."""
+    device tensors; ids_out (int32), scores_out (float32) hold k + 1 entries,
+    n_out and status_out (int32) one each, all on the device.  query_kp:
+    host, 17 x 2."""
     import numpy as np
     kp = np.ascontiguousarray(np.asarray(query_kp, dtype=np.float32).reshape(34))
     _check(load().la_pose_topk_noalloc(
         _ptr(table), _ptr(inv_norm), int(table.shape[0]),
         kp.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), pose_row, c0, c1, k,
-        _ptr(ids_out), _ptr(scores_out), _ptr(n_out), _stream_handle(stream)),
+        _ptr(ids_out), _ptr(scores_out), _ptr(n_out), _ptr(status_out), _stream_handle(stream)),
         "la_pose_topk_noalloc")
 
 

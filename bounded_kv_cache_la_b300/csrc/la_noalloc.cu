@@ -11,7 +11,9 @@
 //   [64, 256)          DevTopk   (CTA completion counter + ranked results)
 //   [256, 256 + 4*N)   per-candidate scores, N = LA_NOALLOC_MAX_ROWS
 // The header must start at zero on every call (the completion counter and
-// the error word); the scores are written before they are read.
+// the error word); the ranked ids start at -1, so ranks past the number of
+// candidates read -1 rather than a stale or zero id; the scores are written
+// before they are read.
 #include <cstddef>
 #include <mutex>
 
@@ -59,12 +61,15 @@ cudaError_t scratch_address(char** out) {
 extern "C" la_status la_pose_topk_noalloc(float* table, float* inv_norm, int max_rows,
                                           const float* query_kp, int pose_row, int c0, int c1,
                                           int k, int32_t* ids_out, float* scores_out,
-                                          int32_t* n_out, void* stream) {
-  if (!table || !inv_norm || !query_kp || !ids_out || !scores_out || !n_out)
+                                          int32_t* n_out, int32_t* status_out, void* stream) {
+  if (!table || !inv_norm || !query_kp || !ids_out || !scores_out || !n_out || !status_out)
     return LA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(table) & 15) return LA_ERR_INVALID_ARG;
   if (max_rows < 1 || pose_row < -1 || pose_row >= max_rows) return LA_ERR_INVALID_ARG;
   if (c0 < 0 || c1 < c0 || c1 > max_rows) return LA_ERR_INVALID_ARG;
+  // The query's row is written by one CTA while every CTA may be scoring the
+  // candidates, so it must not be one of them.
+  if (pose_row >= c0 && pose_row < c1) return LA_ERR_INVALID_ARG;
   if (c1 > LA_NOALLOC_MAX_ROWS) return LA_ERR_INVALID_ARG;   // beyond the fixed scratch
   if (k < 0 || k > LA_MAX_TOPK) return LA_ERR_INVALID_ARG;
   for (int i = 0; i < 34; ++i)
@@ -74,7 +79,10 @@ extern "C" la_status la_pose_topk_noalloc(float* table, float* inv_norm, int max
   char* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return LA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(base, 0, kHeaderBytes, s) != cudaSuccess) return LA_ERR_CUDA;
+  if (cudaMemsetAsync(base, 0, kHeaderBytes, s) != cudaSuccess ||
+      cudaMemsetAsync(base + kTopkOff + offsetof(DevTopk, ids), 0xFF,
+                      sizeof(int32_t) * (LA_MAX_TOPK + 1), s) != cudaSuccess)
+    return LA_ERR_CUDA;
 
   RetrievalArgs a{};
   for (int i = 0; i < 34; ++i) a.kp[i] = query_kp[i];
@@ -98,6 +106,8 @@ extern "C" la_status la_pose_topk_noalloc(float* table, float* inv_norm, int max
       cudaMemcpyAsync(scores_out, topk + offsetof(DevTopk, scores), sizeof(float) * n_rank,
                       cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(n_out, topk + offsetof(DevTopk, n), sizeof(int32_t),
+                      cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(status_out, base + kErrOff + offsetof(DevError, code), sizeof(int32_t),
                       cudaMemcpyDeviceToDevice, s) != cudaSuccess)
     return LA_ERR_CUDA;
   return LA_OK;

@@ -317,28 +317,42 @@ const char* la_status_string(la_status s);
  *          caller builds its history by calling once per block;
  * query_kp host, 17 (x, y) keypoints of the block being generated;
  * pose_row table row that receives the query's descriptor, or -1 for none;
+ *          it may not lie in [c0, c1) (that row would be written while it is
+ *          being scored);
  * [c0, c1) candidate block ids scored against the query (rows already
  *          written); 0 <= c0 <= c1 <= min(max_rows, LA_NOALLOC_MAX_ROWS);
+ *          the ids returned are table rows (absolute, not relative to c0);
  * k        0 .. LA_MAX_TOPK picks; k + 1 entries are ranked so that the gap
  *          score_k - score_(k+1) can be read;
  * ids_out, scores_out  device, k + 1 entries each, in rank order (score
- *          descending, id ascending); n_out device, 1 int32: entries ranked.
+ *          descending, id ascending); ranks at or past *n_out (fewer than
+ *          k + 1 candidates) hold id -1 and score 0;
+ * n_out    device, 1 int32: entries ranked, min(k + 1, c1 - c0);
+ * status_out device, 1 int32: the kernel's error word, LA_OK (0) or the
+ *          la_status of a fault it detected (the host checks above reject
+ *          every input the kernel would fault on, so it reads LA_OK unless
+ *          the library itself is wrong).
  *
  * Sizes beyond the scratch (c1 > LA_NOALLOC_MAX_ROWS) are rejected with
  * LA_ERR_INVALID_ARG before any work is enqueued, as are bad pointers and
- * ranges.  The call enqueues a memset of the scratch header, the kernel and
- * three device-to-device copies on `stream`, and does not synchronise.  It
- * calls no cudaMalloc, cudaFree or other allocating routine.  Its first
+ * ranges.  The call enqueues two memsets of the scratch header, the kernel
+ * and four device-to-device copies on `stream`, and does not synchronise.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  Its first
  * call on a device (with that device current) looks up the scratch array's
- * device address; make that first call before any stream capture.  Every
- * call shares the one array and it keeps the last call's contents: calls
- * that overlap on the GPU (different streams, no ordering) race and give
- * wrong results. */
+ * device address, and that lookup, like the first launch of the retrieval
+ * kernel, may load the library's device code, which the CUDA runtime can
+ * allocate memory for: a caller that may not allocate once it is serving
+ * makes one call (or one la_select_context) on each device before it
+ * starts, and before any stream capture.  The address is kept for the life
+ * of the process, so cudaDeviceReset after the first call is not supported.
+ * Every call shares the one array and it keeps the last call's contents:
+ * calls that overlap on the GPU (different streams, no ordering) race and
+ * give wrong results. */
 #define LA_NOALLOC_MAX_ROWS 65536
 la_status la_pose_topk_noalloc(float* table, float* inv_norm, int max_rows,
                                const float* query_kp, int pose_row, int c0, int c1, int k,
                                int32_t* ids_out, float* scores_out, int32_t* n_out,
-                               void* stream);
+                               int32_t* status_out, void* stream);
 
 #ifdef __cplusplus
 }

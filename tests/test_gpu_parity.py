@@ -237,10 +237,13 @@ def test_history_load_rows_equal_retrieval_rows():
     ids = torch.empty(k + 1, dtype=torch.int32, device="cuda")
     scores = torch.empty(k + 1, dtype=torch.float32, device="cuda")
     n_out = torch.empty(1, dtype=torch.int32, device="cuda")
+    status = torch.empty(1, dtype=torch.int32, device="cuda")
     for b in range(n):
-        capi.la_pose_topk_noalloc(table, inv, kps[b], b, 0, 0, 0, ids, scores, n_out)
-    capi.la_pose_topk_noalloc(table, inv, kps[n], n, 1, n - sc.window, k, ids, scores, n_out)
+        capi.la_pose_topk_noalloc(table, inv, kps[b], b, 0, 0, 0, ids, scores, n_out, status)
+    capi.la_pose_topk_noalloc(table, inv, kps[n], n, 1, n - sc.window, k, ids, scores, n_out,
+                              status)
     torch.cuda.synchronize()
+    assert int(status.item()) == capi.LA_OK
     got = sorted(zip(ids.cpu().numpy()[:k].tolist(), scores.cpu().numpy()[:k].tolist()))
     assert [g[0] for g in got] == ctx["dyn_ids"]
     assert [np.float32(g[1]) for g in got] == [np.float32(x) for x in ctx["dyn_scores"]]

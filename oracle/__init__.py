@@ -22,12 +22,25 @@ Where the pages leave a step open, the reading taken is written next to the
 function that takes it.
 
 Parity status of each function (what pins it in tests/test_oracle_*.py):
-  pose.descriptor / pose.cosine_scores / pose.select_topk : pinned
-  rope.*                 : pinned (complex multiplication for the default and
+  pose.descriptor / pose.cosine_scores / pose.select_topk : pinned (scipy
+                           cosine distance, identity / translation / scale,
+                           brute-force top-k with ties, whole-stream brute force)
+  rope.rotate            : pinned (complex multiplication for the default and
                            explicit (t, h, w) splits, norm, identity, shift,
-                           closed form, golden)
+                           closed form)
+  rope.block_positions   : pinned (hand-written raster list)
   attention.softmax_attention : pinned (torch SDPA / scipy softmax, uniform V)
-  stream.*               : pinned (constant KV length, window/sink invariants)
+  stream.plan_*          : pinned (constant KV length, window/sink invariants)
+  stream.context_kv / chunk_attention : pinned (positions typed out by hand
+                           for PR-Sink slots and for the ConvKV memory at
+                           (j, 0, 0); the e4m3 branch reduces to the bf16
+                           branch on exactly representable blocks, and a key
+                           turned twice fails that pin; zero query -> mean of
+                           V; shift / slot-permutation invariance; library
+                           attention without RoPE)
+  stream.rotate_within_block_f32 / fp8_store : pinned (fp64 rotation within
+                           fp32 rounding; per-head scales)
   convkv.*               : pinned (torch conv1d, closed-form weights, FIFO cap)
   e4m3.*                 : pinned (format table, torch float8 cast, RNE ties)
+No function is left unpinned.
 """

@@ -212,3 +212,35 @@ def test_boundary_distance_flags_midpoints():
     mids = (vals[1:] + vals[:-1]) / 2
     assert np.all(e4m3.boundary_distance(mids[5:]) == 0)
     assert np.all(e4m3.boundary_distance(vals[10:]) > 1e-3)
+
+
+def _fp8_tc_golden():
+    out = {}
+    for line in open(os.path.join(GOLDEN, "fp8_tc_error.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        k, v = line.split()
+        out[k] = float(v)
+    return out
+
+
+def test_fp8_tensor_core_tolerance_covers_simulated_rounding():
+    """The e4m3 tensor-core tolerance of the GPU parity tests against the
+    simulated effect of rounding the queries and probabilities to e4m3
+    (tests/golden/make_fp8_tc_error.py, written from the oracle's storage
+    functions): the simulation reproduces the oracle when it does not
+    round, and the bounds cover the rounded result with margin, both on a
+    small sample here and on the larger committed one."""
+    import importlib.util
+    from tests.harness import TOL
+    spec = importlib.util.spec_from_file_location("make_fp8_tc_error",
+                                                  os.path.join(GOLDEN, "make_fp8_tc_error.py"))
+    sim = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(sim)
+    o_ref, o_exact = sim.simulate(heads=(5,), n_rows=32, rounding=False)
+    np.testing.assert_allclose(o_exact, o_ref, rtol=0, atol=1e-9)
+    small = sim.errors(*sim.simulate(heads=(5, 30), n_rows=48))
+    tol = TOL["e4m3_tc"]
+    for e in (small, _fp8_tc_golden()):
+        assert 0.01 < e["rel_l2"] and 1.4 * e["rel_l2"] <= tol["rel"], e
+        assert 10 * e["max_abs"] <= tol["max_abs"] and 10 * e["mean_abs"] <= tol["mean_abs"], e

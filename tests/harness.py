@@ -73,6 +73,61 @@ class Values:
                           self.get(layer, b, step_of_block(b), "v"))
 
 
+class FullValues:
+    """Seeded per-(layer, block, step) Q/K/V with every head, for the oracle
+    at full shapes.  The seeded generator's torch backend draws them (the
+    NumPy backend takes ~13 s per 14B-shape tensor); both backends give
+    bit-identical values, and every tensor drawn here is checked against
+    the NumPy backend on 4096 random elements.  Holds the blocks of the
+    latest context only (prune())."""
+
+    def __init__(self, sc, device="cuda"):
+        self.sc, self.device = sc, device
+        self._cache = {}
+        self._rng = np.random.default_rng(12345)
+
+    def get(self, layer, block, step, which):
+        key = (layer, block, step, which)
+        if key not in self._cache:
+            sc = self.sc
+            T, H, D = sc.tokens_per_block, sc.num_heads, sc.head_dim
+            k = gen.qkv_key(sc, layer, block, step, which)
+            x = gen.tensor_torch(k, (T, H, D), sc.qkv_dtype, self.device).float().cpu().numpy()
+            idx = self._rng.integers(0, x.size, size=4096).astype(np.uint64)
+            ref = gen.tensor_np(k, None, sc.qkv_dtype, index_map=idx)
+            assert np.array_equal(x.reshape(-1)[idx.astype(np.int64)], ref), key
+            self._cache[key] = x
+        return self._cache[key]
+
+    def kv_of(self, layer, step_of_block):
+        return lambda b: (self.get(layer, b, step_of_block(b), "k"),
+                          self.get(layer, b, step_of_block(b), "v"))
+
+    def prune(self, keep_blocks):
+        for key in [k for k in self._cache if k[1] not in keep_blocks]:
+            del self._cache[key]
+
+
+def oracle_output_heads(sc, ctx, vals, layer, step, n_steps, rows=None, w_kv=None, group=8):
+    """oracle_output over every head, computed `group` heads at a time (the
+    oracle's fp64 context for all 40 heads would need several GB at once)."""
+    H = sc.num_heads
+    kv_of = vals.kv_of(layer, lambda b: step if b == ctx.block else n_steps - 1)
+    q = vals.get(layer, ctx.block, step, "q")
+    out = None
+    for h0 in range(0, H, group):
+        hs = slice(h0, min(H, h0 + group))
+        kv_h = lambda b, hs=hs: tuple(x[:, hs] for x in kv_of(b))
+        mem = None
+        if ctx.mem_tokens:
+            mem = ostream.convkv_memory(sc, ctx.block, kv_h, w_kv[:, hs])
+        o = ostream.chunk_attention(sc, ctx, q[:, hs], kv_h, mem=mem, rows=rows)
+        if out is None:
+            out = np.zeros((o.shape[0], H, o.shape[2]))
+        out[:, hs] = o
+    return out
+
+
 def torch_values(sc, layer, block, step, device="cuda"):
     T, H, D = sc.tokens_per_block, sc.num_heads, sc.head_dim
     return [gen.tensor_torch(gen.qkv_key(sc, layer, block, step, w), (T, H, D), sc.qkv_dtype,

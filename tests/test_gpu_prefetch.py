@@ -1,12 +1,14 @@
-"""Host-memory history tier with fetch-ahead: while block b runs, the
-retrieval of block b + 1 is done early (la_prefetch_context) and the picked
-blocks' K/V are written from page-locked host memory on a separate copy
-stream.  Outputs must be identical to the plain path (retrieval at select,
-fills from device memory), and the dynamic sinks must agree."""
+"""Host-memory history tier with fetch-ahead ("SoulX-LiveAct", 上手实践指南:
+block offload): while block b runs, the retrieval of block b + 1 is done
+early (la_prefetch_context) and the picked blocks' K/V are written from
+page-locked host memory on a separate copy stream.  Outputs must match the
+oracle, be identical to the plain path (retrieval at select, fills from
+device memory), and the dynamic sinks must agree."""
 import numpy as np
 import pytest
 
 from bounded_kv_cache_la_b300 import capi
+from oracle import stream as ostream
 from synth import C3_14B, C5_FP8, gen
 
 from . import harness as H
@@ -90,6 +92,19 @@ def test_fetch_ahead_from_host_matches_plain_path(sc):
     import torch
     for key in plain:
         assert torch.equal(plain[key], fetched[key]), key
+    # the fetched-ahead path against the oracle: a warm-up block, the first
+    # block with a full dynamic sink, the last block; both layers
+    ref = ostream.plan_stream(sc, gen.poses(sc, n_blocks=n + 1), n)
+    first_full = min(b for b in range(n) if len(ref[b].dyn_ids) == sc.dyn_topk)
+    vals = H.Values(sc)
+    kind = "bf16" if sc.kv_dtype == "bf16" else "e4m3_tc"
+    for b in (2, first_full, n - 1):
+        assert dyn_f[b] == ref[b].dyn_ids or ref[b].gap <= 1e-6, (b, dyn_f[b], ref[b])
+        if dyn_f[b] != ref[b].dyn_ids:
+            continue
+        for l in range(2):
+            o = H.oracle_output(sc, ref[b], vals, l, 0, 1)
+            H.compare(fetched[(b, l)].float().cpu().numpy(), o, kind, f"block {b} layer {l}")
 
 
 def test_prefetch_call_rules():

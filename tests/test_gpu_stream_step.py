@@ -1,11 +1,13 @@
 """la_stream_step (one call per block; its last denoising step writes the
-block's pages straight into the block's own frame) against the per-call C
-ABI path on the same inputs: every output and every stored page identical,
-and the per-call path itself against the oracle elsewhere."""
+block's pages straight into the block's own frame) against the oracle on a
+warm-up block, the first block with a full context and the last block, and
+against the per-call C ABI path on the same inputs: every output and every
+stored page identical."""
 import numpy as np
 import pytest
 
 from bounded_kv_cache_la_b300 import capi
+from oracle import stream as ostream
 from synth import C2_MID, C4_CONVKV, C5_FP8, gen
 
 from . import harness as H
@@ -32,10 +34,29 @@ def _tensors(sc, L, S, b):
     return q, k, v
 
 
+def _oracle_plan(sc, kps, n):
+    if sc.policy == "convkv":
+        return [ostream.plan_convkv(sc, b) for b in range(n)]
+    return ostream.plan_stream(sc, kps, n)
+
+
+def _full_context(sc, ref):
+    """First block whose context is complete (full dynamic sink, or a full
+    ConvKV memory)."""
+    if sc.policy == "convkv":
+        return min(c.block for c in ref if c.mem_tokens == sc.mem_slots)
+    return min(c.block for c in ref if len(c.dyn_ids) == sc.dyn_topk)
+
+
 def _compare(sc, n, L=2, S=2):
     import torch
     scl = sc.with_(num_layers=L)
     kps = gen.poses(sc, n_blocks=n)
+    ref = _oracle_plan(sc, kps, n)
+    checks = {2, _full_context(sc, ref), n - 1}
+    vals = H.Values(sc)
+    w = [gen.conv_weights_np(sc, l) for l in range(L)] if sc.policy == "convkv" else [None] * L
+    kind = "e4m3_tc" if sc.kv_dtype == "e4m3" else "bf16"
     pose = lambda b: kps[b] if sc.policy == "prsink" else np.zeros((17, 2), np.float32)
     fill = lambda layer, blk: tuple(H.torch_values(sc, layer, blk, S - 1)[1:])
     fused, percall = H.make_cache(scl, attn_impl=1), H.make_cache(scl, attn_impl=1)
@@ -57,6 +78,15 @@ def _compare(sc, n, L=2, S=2):
         torch.cuda.synchronize()
         for i in range(S * L):
             assert torch.equal(out_f[i], out_p[i]), (b, i)
+        if b in checks:
+            assert ctx["kv_len"] == ref[b].kv_len
+            if sc.policy == "prsink" and ctx["dyn_ids"] != ref[b].dyn_ids:
+                assert ref[b].gap <= 1e-6
+                continue
+            for i in range(S * L):
+                s_, l = divmod(i, L)
+                o = H.oracle_output(sc, ref[b], vals, l, s_, S, w_kv=w[l])
+                H.compare(out_f[i].float().cpu().numpy(), o, kind, f"block {b} step {s_} layer {l}")
     for cache in (fused, percall):
         st, msg = cache.la_get_error()
         assert st == capi.LA_OK, msg
@@ -82,4 +112,6 @@ def test_stream_step_matches_per_call_e4m3_external():
 
 
 def test_stream_step_matches_per_call_convkv():
-    _compare(C4_CONVKV.with_(num_heads=4, grid_h=5, grid_w=9, mem_slots=240), 12)
+    # 135 tokens per block -> 27 compressed per eviction: the 240-slot memory
+    # is full from block 12
+    _compare(C4_CONVKV.with_(num_heads=4, grid_h=5, grid_w=9, mem_slots=240), 14)

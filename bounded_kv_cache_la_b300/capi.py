@@ -31,6 +31,7 @@ EXPORTS = (
     "la_debug_page", "la_debug_memory", "la_set_profile_events", "la_launch_count",
     "la_status_string", "la_pose_topk_noalloc", "la_refresh_sink", "la_prefetch_context",
     "la_debug_inject", "la_cache_state_bytes", "la_cache_save_state", "la_cache_restore",
+    "la_attention_schedule",
 )
 LA_INJECT_ATTN_STALL = 1
 LA_INJECT_BAD_FRAME = 2
@@ -133,6 +134,7 @@ def load() -> ctypes.CDLL:
         "la_status_string": (ctypes.c_char_p, [i32]),
         "la_pose_topk_noalloc": (i32, [vp, vp, i32, ctypes.POINTER(ctypes.c_float), i32, i32, i32,
                                        i32, vp, vp, vp, vp, vp]),
+        "la_attention_schedule": (i32, [i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -216,6 +218,17 @@ def la_pose_topk_noalloc(table, inv_norm, query_kp, pose_row, c0, c1, k, ids_out
         kp.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), pose_row, c0, c1, k,
         _ptr(ids_out), _ptr(scores_out), _ptr(n_out), _ptr(status_out), _stream_handle(stream)),
         "la_pose_topk_noalloc")
+
+
+def la_attention_schedule(T: int, H: int, num_sms: int):
+    """Host only: the unit dealt at each position by the tensor-core
+    attention (list of ints)."""
+    n_max = H * ((T + 255) // 256)
+    buf = (ctypes.c_int32 * max(1, n_max))()
+    n = load().la_attention_schedule(T, H, num_sms, buf, n_max)
+    if n < 0:
+        raise LaError(LA_ERR_INVALID_ARG, "la_attention_schedule")
+    return list(buf[:n])
 
 
 def _stream_handle(stream) -> ctypes.c_void_p:

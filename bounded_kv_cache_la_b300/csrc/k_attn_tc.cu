@@ -19,10 +19,13 @@
 //
 // Work units.  A unit is (head, pair of 128-row query tiles).  When a head
 // has an odd number of query tiles its last unit is a half unit (one tile).
-// Units are ordered full units first, half units last, and dealt to the
-// persistent CTAs in a snake order (CTA c takes index i*G + c on even rounds
-// and i*G + G-1-c on odd rounds), so that the CTAs that get an extra half
-// unit are the ones that got fewer full units.
+// Positions are dealt to the persistent CTAs in a snake order (CTA c takes
+// position i*G + c on even rounds and i*G + G-1-c on odd rounds), and a
+// table built on the host says which unit sits at each position: full units
+// in head order, and each half unit at a position of a CTA that got fewer
+// full units, in the round where its head's full units run, so that it
+// reads its head's K/V from L2 with them rather than from DRAM in a last
+// wave of its own.
 //
 // CTA = 12 warps, persistent:
 //   warp 0       TMA producer (K ring, V ring, per-slot Q boxes, double-buffered)
@@ -42,11 +45,14 @@
 // a tree of 3-input maxes.  Scale-and-subtract and
 // the row sum use packed fp32x2 arithmetic; the exponentials run on the MUFU
 // unit (ex2.approx).  P is rounded to bf16 (relative error 2^-9) before the
-// PV product.
+// PV product (e4m3 with e4m3 operands).
 //
 // Every wait is bounded (2 s, or the injected limit); on timeout the kernel
 // latches LA_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM
 // and returns.
+#include <algorithm>
+#include <vector>
+
 #include "dev_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -132,21 +138,25 @@ struct Wait {
   }
 };
 
-// Work units: full (head, tile pair) units first, then one half unit per
-// head when the head has an odd number of query tiles.
+// Work units: full (head, tile pair) units h * n_full + p, then one half
+// unit H * n_full + h per head when the head has an odd number of query
+// tiles.  sched[position] is the unit dealt at that position.
 struct Units {
   int H, n_full, n_units;
-  __device__ Units(int T, int H_) : H(H_) {
+  const int* sched;
+  __device__ Units(int T, int H_, const int* sched_) : H(H_), sched(sched_) {
     const int nt_q = (T + kBM - 1) / kBM;
     n_full = nt_q / 2;
     n_units = H * n_full + ((nt_q & 1) ? H : 0);
   }
-  // CTA c's i-th unit index in snake order (may be >= n_units: done).
+  // CTA c's i-th position in snake order (may be >= n_units: done).
   __device__ __forceinline__ int index(int i) const {
     const int G = gridDim.x, c = blockIdx.x;
     return i * G + ((i & 1) ? (G - 1 - c) : c);
   }
-  __device__ __forceinline__ void get(int u, int& h, int& row0, bool& half) const {
+  // The unit at position pos (< n_units).
+  __device__ __forceinline__ void get(int pos, int& h, int& row0, bool& half) const {
+    const int u = __ldg(sched + pos);
     const int nf = H * n_full;
     if (u < nf) {
       h = u / n_full;
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const Wait wait{&ctl.abort_flag, a.err, a.timeout_ns};
   const uint64_t limit_ns = a.timeout_ns;
   const uint32_t tmem = ctl.tmem_base;
-  const Units units(a.T, a.H);
+  const Units units(a.T, a.H, a.sched);
   if (bad && tid == 0) record_error(a.err, LA_ERR_DEVICE, KID_ATTN_TC, n_slots, -1);
 
   if (warp < 4) {
@@ -648,6 +658,42 @@ bool attn_tc_supported(int D, int kv_dtype) {
   return D == kD && (kv_dtype == LA_BF16 || kv_dtype == LA_E4M3);
 }
 
+int attn_tc_units(int T, int H) { return H * ((T + 2 * kBM - 1) / (2 * kBM)); }
+
+static int attn_tc_grid(int T, int H, int num_sms) {
+  const int units = attn_tc_units(T, H);
+  return units < num_sms ? units : num_sms;
+}
+
+// Walks the positions in snake order.  Every CTA keeps the number of half
+// units the plain order (full units first) would give it, so the work per
+// CTA is unchanged; a half unit is placed once its head's full units have
+// started, or when the CTA has no other position left for it.
+void attn_tc_schedule(int T, int H, int num_sms, int* sched) {
+  const int n_full = (T + kBM - 1) / kBM / 2;
+  const int n_units = attn_tc_units(T, H), n_full_total = H * n_full;
+  const int G = attn_tc_grid(T, H, num_sms);
+  std::vector<int> cta(n_units), need_half(G, 0), left(G, 0);
+  for (int p = 0; p < n_units; ++p) {
+    const int i = p / G, k = p - i * G;
+    cta[p] = (i & 1) ? G - 1 - k : k;
+    ++left[cta[p]];
+    if (p >= n_full_total) ++need_half[cta[p]];
+  }
+  int fi = 0, hi = 0;
+  for (int p = 0; p < n_units; ++p) {
+    const int c = cta[p];
+    const int heads_started = n_full > 0 ? std::min(H, (fi + n_full - 1) / n_full) : H;
+    if (need_half[c] > 0 && (left[c] == need_half[c] || hi < heads_started)) {
+      sched[p] = n_full_total + hi++;
+      --need_half[c];
+    } else {
+      sched[p] = fi++;
+    }
+    --left[c];
+  }
+}
+
 template <bool F8>
 static cudaError_t launch_attn_tc_t(const TcAttnArgs& a, int num_sms, cudaStream_t s) {
   // the shared-memory opt-in is a per-device function attribute
@@ -662,9 +708,7 @@ static cudaError_t launch_attn_tc_t(const TcAttnArgs& a, int num_sms, cudaStream
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int n_pairs = (a.T + 2 * kBM - 1) / (2 * kBM);
-  const int units = a.H * n_pairs;
-  const int grid = units < num_sms ? units : num_sms;
+  const int grid = attn_tc_grid(a.T, a.H, num_sms);
   attn_tc_kernel<F8><<<grid, kThreads, Tile<F8>::kSmem, s>>>(a);
   count_launches(1);
   return cudaGetLastError();

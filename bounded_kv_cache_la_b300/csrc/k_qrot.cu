@@ -16,7 +16,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kTokensPerCta = 16;       // full rows
-constexpr int kSplitTokensPerCta = 32;  // split rows
+constexpr int kSplitTokensPerCta = 64;  // split rows
 
 // Loads t0_cur - t0_s of every slot into s_dq and checks that each slot's
 // temporal offset stays inside the RoPE table for every frame of the block.
@@ -158,10 +158,11 @@ __global__ void __launch_bounds__(256) qrot_kernel(QrotArgs a) {
 // Split rows (bf16, every temporal dim below D/2): each slot gets the first
 // half of every row, turned for that slot; the second half, the same for
 // every slot, is written once at slot index n_qrot.
-// Grid: x = tile of 32 tokens, y = head.  A thread takes 8 dims of two
-// neighbouring tokens a, b: warps 0-3 the first halves, warps 4-7 the
-// second halves.  Tokens a and b normally share a frame, hence a table row:
-// the temporal pairs of both then turn together in packed fp32x2,
+// Grid: x = tile of 64 tokens, y = head.  A thread takes 8 dims of each half
+// of two neighbouring tokens a, b: it stores their second halves once, then
+// their first halves for every slot, so every warp runs the slot loop.
+// Tokens a and b normally share a frame, hence a table row: the temporal
+// pairs of both then turn together in packed fp32x2,
 //   y0 = fma(-x1, s, x0 c),  y1 = fma(x0, s, x1 c),
 // with (c, c) and (s, s) from one 16-byte load of the (cos, cos, sin, sin)
 // table; a pair that straddles a frame boundary does the same per token.
@@ -196,35 +197,41 @@ __device__ __forceinline__ void turn_static(const QrotArgs& a, int t, int d0, co
   }
 }
 
-// 4 CTAs per SM (at most 64 registers) keep more Q loads in flight: 62.6 vs
-// 65.1 us per 14B-shape call with the compiler's own 74 registers.
+// 4 CTAs per SM (at most 64 registers) keep more Q loads in flight.
 __global__ void __launch_bounds__(256, 4) qrot_split_kernel(QrotArgs a) {
   __shared__ int s_dq[kMaxAttnSlots];                 // t0_cur - t0_s
   if (!slot_offsets(a, s_dq)) return;
   const int n_slots = a.ctx->n_slots;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
-  const int ta = blockIdx.x * kSplitTokensPerCta + 2 * ((warp & 3) * 4 + (lane >> 3));
+  const int ta = blockIdx.x * kSplitTokensPerCta + 2 * (threadIdx.x >> 3);
   const int tb = ta + 1;
   if (ta >= a.T) return;
   const bool has_b = tb < a.T;
   const int half = a.D / 2;
-  const int d0 = (warp >= 4 ? half : 0) + (lane & 7) * 8;
+  const int d0 = (threadIdx.x & 7) * 8;               // this thread's dims in each half
+  const size_t row_a = ((size_t)h * a.T + ta) * half;   // row of token a in one copy
   float xa[8], xb[8], ya[8], yb[8];
-  load_row8(a, ta, h, d0, xa);
-  if (has_b) load_row8(a, tb, h, d0, xb);
-  else
+  {                                                    // the shared second half, once
+    load_row8(a, ta, h, half + d0, xa);
+    if (has_b) load_row8(a, tb, h, half + d0, xb);
+    load_row8(a, ta, h, d0, ya);                       // first half, loaded early
+    if (has_b) load_row8(a, tb, h, d0, yb);
+    float za[8], zb[8];
+    turn_static(a, ta, half + d0, xa, za);
+    const size_t off = (size_t)a.n_qrot * a.H * a.T * half + row_a + d0;
+    store_row8(a.qrot, off, za);
+    if (has_b) {
+      turn_static(a, tb, half + d0, xb, zb);
+      store_row8(a.qrot, off + half, zb);
+    }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) xb[e] = 0.f;
+    for (int e = 0; e < 8; ++e) {
+      xa[e] = ya[e];
+      xb[e] = has_b ? yb[e] : 0.f;
+    }
+  }
   turn_static(a, ta, d0, xa, ya);
   turn_static(a, has_b ? tb : ta, d0, xb, yb);
-  const size_t row_a = ((size_t)h * a.T + ta) * half;   // row of token a in one copy
-  if (d0 >= half) {                                    // the shared second half, once
-    const size_t off = (size_t)a.n_qrot * a.H * a.T * half + row_a + (d0 - half);
-    store_row8(a.qrot, off, ya);
-    if (has_b) store_row8(a.qrot, off + half, yb);
-    return;
-  }
   const int fa = (int)fdiv((uint32_t)ta, a.rope.div_hw);
   const int fb = has_b ? (int)fdiv((uint32_t)tb, a.rope.div_hw) : fa;
   const int pairs_t = a.rope.dt >> 1, pair0 = d0 >> 1;

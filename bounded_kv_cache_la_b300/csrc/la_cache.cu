@@ -58,6 +58,7 @@ struct la_cache {
   bool tc = false;
   bool q_split = false;          // split rotated-query layout (see QrotArgs)
   CUtensorMap tm_q{}, tm_kv{}, tm_cur{}, tm_mem{};
+  std::vector<int> sched;           // tensor path: unit at each dealt position (uploaded)
   int num_sms = 148;
   std::vector<cudaEvent_t> prof_start, prof_stop;
   int inject_stall = 0;             // tensor-core launches still to stall (tests)
@@ -190,6 +191,7 @@ void compute_layout(const la_cache_config& c, Layout& L) {
   const bool f8 = c.kv_dtype == LA_E4M3;
   L.qrot = take(tc ? (size_t)L.n_qrot * H * T * D * (f8 ? 1 : 2) : 0);
   L.qscale = take(tc && f8 ? sizeof(float) * (size_t)H * T : 0);
+  L.sched = take(tc ? sizeof(int) * (size_t)attn_tc_units(T, H) : 0);
   L.rope_t2 = take(tc && !f8 ? sizeof(float4) * (size_t)L.max_t * (c.rope_t / 2 > 0 ? c.rope_t / 2 : 1) : 0);
   L.mem = take(is_prsink(c) ? 0 : (size_t)c.num_layers * 3 * H * c.mem_slots * D * 2);
   L.total = off;
@@ -504,6 +506,16 @@ la_status la_context_plan(const la_cache_config* cfg, int block, const int32_t* 
   return LA_OK;
 }
 
+int la_attention_schedule(int T, int H, int num_sms, int32_t* out, int cap) {
+  if (T < 1 || T > kMaxBlockTokens || H < 1 || H > 64 || num_sms < 1 || !out) return -1;
+  const int n = attn_tc_units(T, H);
+  if (cap < n) return -1;
+  std::vector<int> sched((size_t)n);
+  attn_tc_schedule(T, H, num_sms, sched.data());
+  for (int i = 0; i < n; ++i) out[i] = sched[i];
+  return n;
+}
+
 // Builds the cache object over the caller's pool; init_pool: zero the
 // control and ring regions and build the RoPE tables (a restored pool
 // already holds them).
@@ -593,6 +605,15 @@ static la_status create_cache(const la_cache_config* cfg, void* dev_pool, size_t
       c->failed = true;
       st = LA_ERR_CUDA;
       c->last_msg = "cuTensorMapEncodeTiled failed";
+    }
+    // the work-unit table depends on this device's SM count: built on every
+    // create, a restored pool included
+    if (st == LA_OK) {
+      c->sched.resize((size_t)attn_tc_units(c->T, H));
+      attn_tc_schedule(c->T, H, c->num_sms, c->sched.data());
+      st = cuda_status(c, cudaMemcpyAsync(c->pool + L.sched, c->sched.data(),
+                                          sizeof(int) * c->sched.size(), cudaMemcpyHostToDevice, s),
+                       "upload work-unit table");
     }
   }
   if (st != LA_OK) {
@@ -1020,6 +1041,7 @@ la_status chunk_attention(la_cache* c, int layer, const void* q, const void* k_c
     ta.tm_cur = c->tm_cur;
     ta.tm_mem = c->tm_mem;
     ta.ctx = dctx;
+    ta.sched = reinterpret_cast<const int*>(c->pool + c->L.sched);
     ta.kv_f8 = g.kv_dtype == LA_E4M3;
     ta.q_shared_z = c->q_split ? c->L.n_qrot * g.num_heads : -1;
     ta.frame_scales = ta.kv_f8 ? frame_scales(c, layer, 0) : nullptr;

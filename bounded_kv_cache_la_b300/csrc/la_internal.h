@@ -67,6 +67,7 @@ struct Layout {
   size_t rope_t2;                  // bf16 tensor path: temporal table as (cos, cos, sin, sin)
   size_t ctx_inject;               // slot table of an injected failure (la_debug_inject)
   size_t qscale;                   // e4m3 tensor path: [H][T] fp32 query scales
+  size_t sched;                    // tensor path: [work units] unit at each dealt position
   size_t mem;                      // ConvKV [L][3][H][cap][D] bf16 (raw K, V, rotated K)
   size_t total;
   size_t page_bytes;               // H * T * D * elt(kv_dtype)
@@ -204,6 +205,8 @@ struct TcAttnArgs {
   CUtensorMap tm_cur;  // current pages    [2*H][T][D]
   CUtensorMap tm_mem;  // ConvKV rings     [L*3*H][cap][D] (or a dummy)
   const DevContext* ctx;
+  const int* sched;           // [H * ceil(T / 256)] unit dealt at each position
+                              // (attn_tc_schedule for the launch's grid)
   const float* frame_scales;  // e4m3: this layer's [n_frames][2][H]
   const float* cur_scales;    // e4m3: [2][H]
   const float* q_scales;      // e4m3: [H][T]
@@ -223,6 +226,10 @@ struct TcAttnArgs {
   DevError* err;
 };
 cudaError_t launch_attn_tc(const TcAttnArgs& a, int num_sms, cudaStream_t s);
+// Work units and the table of the unit dealt at each position, for the grid
+// launch_attn_tc uses with num_sms SMs.
+int attn_tc_units(int T, int H);
+void attn_tc_schedule(int T, int H, int num_sms, int* sched);
 bool attn_tc_supported(int D, int kv_dtype);
 
 }  // namespace la

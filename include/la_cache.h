@@ -254,6 +254,17 @@ la_status la_get_error(la_cache_t* cache, char* msg, size_t cap);
 la_status la_context_plan(const la_cache_config* cfg, int block, const int32_t* dyn_ids,
                           int n_dyn, la_context* out);
 
+/* Host only, no device work: how the tensor-core attention deals its work
+ * units to a device with `num_sms` SMs, for blocks of T tokens and H heads.
+ * A unit is (head, pair of 128-row query tiles), numbered h * n_full + p;
+ * a head with an odd number of query tiles adds a half unit (one tile),
+ * numbered H * n_full + h.  out[pos] (host, `cap` entries) receives the unit
+ * dealt at position pos; positions go to the SMs in snake order (SM c takes
+ * positions i * G + c on even rounds i and i * G + G - 1 - c on odd ones,
+ * G = min(units, num_sms)).  Returns the number of units, or -1 for bad
+ * arguments or a short buffer. */
+int la_attention_schedule(int T, int H, int num_sms, int32_t* out, int cap);
+
 /* Test access to stored pages.  Returns the device address of the page
  * holding `which` (0 = RoPE'd key, 1 = value, 2 = raw key [ConvKV]) of
  * `block_id` for `layer`, laid out [H][T][D] in kv_dtype, and for e4m3 the

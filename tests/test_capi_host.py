@@ -211,3 +211,39 @@ int main() {
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     checked, bad = map(int, out.stdout.split())
     assert out.returncode == 0 and bad == 0 and checked == 5000 * 4004
+
+
+@pytest.mark.parametrize("T,H,sms", [(4680, 40, 148), (3510, 40, 148), (1560, 12, 148),
+                                     (48, 3, 148), (4680, 64, 148), (4680, 40, 132),
+                                     (390, 4, 148), (4680, 1, 148)])
+def test_attention_schedule_balanced_and_halves_near_their_heads(lib, T, H, sms):
+    """The tensor-core attention's work-unit table: every unit once, the
+    same work per SM as dealing full units first and half units last, and
+    each half unit in a round where its head's full units run (so it reads
+    its head's K/V from L2 with them)."""
+    from bounded_kv_cache_la_b300 import capi
+    sched = capi.la_attention_schedule(T, H, sms)
+    nt = (T + 127) // 128
+    n_full = nt // 2
+    n_units = H * (n_full + (nt & 1))
+    assert sorted(sched) == list(range(n_units))
+    G = min(n_units, sms)
+    cta = [(p % G if (p // G) % 2 == 0 else G - 1 - p % G) for p in range(n_units)]
+    rnd = [p // G for p in range(n_units)]
+    work = lambda u: 1.0 if u < H * n_full else 0.5
+    load, plain = [0.0] * G, [0.0] * G
+    for p, u in enumerate(sched):
+        load[cta[p]] += work(u)
+        plain[cta[p]] += work(p)
+    assert load == plain
+    full_rounds = {}
+    for p, u in enumerate(sched):
+        if u < H * n_full:
+            full_rounds.setdefault(u // n_full, []).append(rnd[p])
+    for p, u in enumerate(sched):
+        if u >= H * n_full and n_full > 0:
+            rs = full_rounds[u - H * n_full]
+            assert min(rs) - 1 <= rnd[p] <= max(rs) + 1, (u, rnd[p], rs)
+    assert capi.la_attention_schedule.__doc__
+    with pytest.raises(capi.LaError):
+        capi.la_attention_schedule(0, H, sms)

@@ -189,14 +189,41 @@ def oracle_one_thread():
                       "seconds": dt}), flush=True)
 
 
+def oracle_full_calls():
+    """The oracle over whole calls of the tiny and mid streams (every head
+    and query row of block 10, full context), inputs generated beforehand
+    and not timed; best of 3."""
+    from oracle import stream as ostream
+    from synth import C1_TINY, C2_MID, gen
+    res = {}
+    for sc in (C1_TINY, C2_MID):
+        T, H, D = sc.tokens_per_block, sc.num_heads, sc.head_dim
+        b = 10
+        ctx = ostream.plan_stream(sc, gen.poses(sc, n_blocks=b + 1), b + 1)[b]
+        val = {(blk, w): gen.tensor_np(gen.qkv_key(sc, 0, blk, 0, w), (T, H, D), sc.qkv_dtype)
+               for blk in ctx.blocks for w in ("q", "k", "v")}
+        kv_of = lambda blk: (val[(blk, "k")], val[(blk, "v")])
+        times = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            ostream.chunk_attention(sc, ctx, val[(b, "q")], kv_of)
+            times.append(time.perf_counter() - t0)
+        fl = attn_flops(sc, ctx.kv_len)
+        res[sc.name] = {"call_s": min(times), "tflops": fl / min(times) / 1e12, "kv_len": ctx.kv_len,
+                        "sample": f"one whole call (block {b}, all {H} heads x {T} rows), fp64 NumPy"}
+    return res
+
+
 def cpu_baseline():
     """The oracle on the host cores: the bounded 14B-shape sample with every
-    BLAS thread, and (in a child process whose BLAS is limited to one thread
-    before NumPy loads) a smaller sample on one thread."""
+    BLAS thread, whole calls of the tiny and mid streams, and (in a child
+    process whose BLAS is limited to one thread before NumPy loads) a smaller
+    sample on one thread."""
     smp = OracleSample(workload())
     dt = min(smp.run() for _ in range(3))          # ~10 s of CPU work on 16 cores
     out = {"value": smp.flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
-           "kind": "oracle", "sample": smp.text, "seconds": dt}
+           "kind": "oracle", "sample": smp.text, "seconds": dt,
+           "full_calls": oracle_full_calls()}
     try:
         r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-thread"],
                            capture_output=True, text=True, timeout=300,
@@ -479,6 +506,53 @@ def host_tier_leg(torch, capi, gen, q, k, v, out, bank, ahead, n_time=3):
     return float(np.median([marks[t].elapsed_time(marks[t + 1]) for t in range(n_time)]))
 
 
+def small_stream_leg(torch, capi, gen, sc, b0=10, calls=50):
+    """Per-call time of the tiny and mid streams (all heads, seeded Q/K/V):
+    blocks 0..b0-1 streamed through the per-call C ABI, then `calls`
+    attention calls of block b0 timed with CUDA events (kernel alone, and the
+    whole call: current pages, query rotation and attention)."""
+    T, H, D = sc.tokens_per_block, sc.num_heads, sc.head_dim
+    cache = capi.Cache(capi.config_for(sc.with_(num_layers=1)))
+    kps = gen.poses(sc, n_blocks=b0 + 1)
+    val = lambda b, w: gen.tensor_torch(gen.qkv_key(sc, 0, b, 0, w), (T, H, D), sc.qkv_dtype, "cuda")
+    for b in range(b0):
+        cache.la_select_context(kps[b])
+        q, k, v = val(b, "q"), val(b, "k"), val(b, "v")
+        out = torch.empty_like(q)
+        cache.la_chunk_attention(0, q, k, v, out)
+        cache.la_cache_append_block(0, k, v)
+    ctx = cache.la_select_context(kps[b0])
+    q, k, v = val(b0, "q"), val(b0, "k"), val(b0, "v")
+    out = torch.empty_like(q)
+    for _ in range(5):
+        cache.la_chunk_attention(0, q, k, v, out)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(calls)]
+    for a_, b_ in ev:
+        a_.record(); b_.record()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    cache.la_set_profile_events([a_.cuda_event for a_, _ in ev], [b_.cuda_event for _, b_ in ev])
+    marks[0].record()
+    for _ in range(calls):
+        cache.la_chunk_attention(0, q, k, v, out)
+    marks[1].record()
+    torch.cuda.synchronize()
+    cache.la_set_profile_events([], [])
+    st, msg = cache.la_get_error()
+    if st != capi.LA_OK:
+        raise RuntimeError(msg)
+    cache.close()
+    attn_ms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in ev]))
+    call_ms = marks[0].elapsed_time(marks[1]) / calls
+    fl = attn_flops(sc, ctx["kv_len"])
+    return {"kv_len": ctx["kv_len"], "block": b0, "flop_per_call": fl,
+            "kernel": "attn_simt_kernel (fp32)" if sc.qkv_dtype == "f32" else "attn_tc_kernel (bf16)",
+            "attn_call_ms": attn_ms, "whole_call_ms": call_ms,
+            "attn_tflops": fl / (attn_ms / 1e3) / 1e12, "call_tflops": fl / (call_ms / 1e3) / 1e12,
+            "note": "inputs resident; L2 holds the whole context at this size"}
+
+
 def extra_legs(torch, capi, gen, q, k, v, out, bank, main_block_ms, pk):
     """FP8 stress stream, ConvKV stream and the latency-flatness check."""
     from synth import C3_14B, C4_CONVKV, C5_FP8
@@ -562,7 +636,10 @@ def extra_legs(torch, capi, gen, q, k, v, out, bank, main_block_ms, pk):
                 "layers x 96 MB per block) then filled; device-memory history = the main leg",
         "fills_at_select_block_ms": at_select, "fetched_ahead_block_ms": fetched,
         "device_history_block_ms": float(np.median(main_block_ms))}
+    from synth import C1_TINY, C2_MID
     res["variants"] = {
+        "c1_tiny": small_stream_leg(torch, capi, gen, C1_TINY),
+        "c2_mid": small_stream_leg(torch, capi, gen, C2_MID),
         "c5_fp8": fp8,
         "c3_14b_e4m3": c3f8,
         "c4_convkv": {"kv_len": kv4, "blocks": "10-12", "block_ms": float(np.median(bms)),
@@ -659,19 +736,20 @@ def run_ours(a):
     if sc.policy == "convkv":
         conv_w = torch.stack([gen.conv_weights_torch(sc, l, "cuda") for l in range(L)]).contiguous()
     cache = capi.Cache(cfg, conv_w=conv_w)
-    g = torch.Generator(device=dev)
-    g.manual_seed(1234 + rank)
+    scr = sc.with_(seed=sc.seed + 1000 * rank)      # each replica its own values
 
-    def randn():
-        return torch.randn((T, H, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    def seeded(layer, block, step, which):
+        """The parity tests' seeded generator (Irwin-Hall(4), mean 0,
+        variance 1, bf16), drawn on the device."""
+        return gen.tensor_torch(gen.qkv_key(scr, layer, block, step, which), (T, H, D), "bf16", dev)
 
     # resident inputs: Q/K/V per (layer, step); outputs per layer
-    q = [[randn() for _ in range(S)] for _ in range(L)]
-    k = [[randn() for _ in range(S)] for _ in range(L)]
-    v = [[randn() for _ in range(S)] for _ in range(L)]
+    q = [[seeded(l, 0, s, "q") for s in range(S)] for l in range(L)]
+    k = [[seeded(l, 0, s, "k") for s in range(S)] for l in range(L)]
+    v = [[seeded(l, 0, s, "v") for s in range(S)] for l in range(L)]
     out = [torch.empty((T, H, D), dtype=torch.bfloat16, device=dev) for _ in range(L)]
     # the caller's history store: block id -> bank entry (id mod 4), per layer
-    bank = [[(randn(), randn()) for _ in range(4)] for _ in range(L)]
+    bank = [[(seeded(l, 1 + i, 0, "k"), seeded(l, 1 + i, 0, "v")) for i in range(4)] for l in range(L)]
 
     if external:
         cache.la_cache_load_history(kps[:b0].reshape(b0, 34))
@@ -898,7 +976,7 @@ def run_ours(a):
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": t_max / a.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3" if sc.kv_dtype == "e4m3" else "bf16",
-            "data": "synthetic (seeded torch.randn Q/K/V, synthetic pose stream)",
+            "data": "synthetic (seeded counter-hash Q/K/V as in the parity tests, synthetic pose stream)",
             "config": workload_desc(sc, b0 + a.warmup, a.steps) | {"parallelism": f"replicas x{world}"},
             "blocks_per_s": blocks_per_s,
             "per_block_latency_ms": t_max / a.steps * 1e3,

@@ -88,6 +88,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int elt_size(int dtype) { return dtype == LA_F32 ? 4 : dtype == LA_BF16 ? 2 : 1; }
 
 bool is_prsink(const la_cache_config& c) { return c.policy == LA_POLICY_PR_SINK; }
+// The kernels move Q/K/V/O rows and conv weights in 16-byte vectors.
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 bool is_external(const la_cache_config& c) { return c.history_mode == LA_HISTORY_EXTERNAL; }
 
 la_status validate(const la_cache_config* c) {
@@ -526,7 +528,7 @@ static la_status create_cache(const la_cache_config* cfg, void* dev_pool, size_t
   la_status st = validate(cfg);
   if (st != LA_OK) return st;
   if (!dev_pool || (reinterpret_cast<uintptr_t>(dev_pool) & 255)) return LA_ERR_INVALID_ARG;
-  if (cfg->policy == LA_POLICY_CONVKV && !conv_w) return LA_ERR_INVALID_ARG;
+  if (cfg->policy == LA_POLICY_CONVKV && (!conv_w || !aligned16(conv_w))) return LA_ERR_INVALID_ARG;
   Layout L;
   compute_layout(*cfg, L);
   if (pool_bytes < L.total) return LA_ERR_OOM;
@@ -851,7 +853,8 @@ la_status la_fill_block(la_cache_t* c, int layer, int block_id, const void* k, c
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
   if (!is_prsink(g) || !is_external(g)) return LA_ERR_UNSUPPORTED;
-  if (layer < 0 || layer >= g.num_layers || !k || !v) return LA_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= g.num_layers || !k || !v || !aligned16(k) || !aligned16(v))
+    return LA_ERR_INVALID_ARG;
   const bool cur = c->selected && contains(c->dyn, block_id);
   const bool ahead = c->pre_for >= c->b && contains(c->pre, block_id);
   if (!cur && !ahead) return c->selected || c->pre_for >= c->b ? LA_ERR_INVALID_ARG : LA_ERR_STATE;
@@ -913,7 +916,8 @@ la_status la_fill_window(la_cache_t* c, int layer, int block_id, const void* k, 
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
   if (!is_prsink(g) || !is_external(g)) return LA_ERR_UNSUPPORTED;
-  if (layer < 0 || layer >= g.num_layers || !k || !v) return LA_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= g.num_layers || !k || !v || !aligned16(k) || !aligned16(v))
+    return LA_ERR_INVALID_ARG;
   std::vector<int> win = window_blocks(g, c->b);
   bool ok = std::find(win.begin(), win.end(), block_id) != win.end() ||
             (g.static_sink && block_id == 0 && c->b >= 1);
@@ -930,7 +934,8 @@ la_status la_refresh_sink(la_cache_t* c, int layer, const void* k, const void* v
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
   if (!is_prsink(g) || !g.static_sink) return LA_ERR_UNSUPPORTED;
-  if (layer < 0 || layer >= g.num_layers || !k || !v) return LA_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= g.num_layers || !k || !v || !aligned16(k) || !aligned16(v))
+    return LA_ERR_INVALID_ARG;
   if (c->selected || c->b < 1 || c->frame_of[0] < 0) return LA_ERR_STATE;
   const int f = c->frame_of[0];
   st = write_pages(c, layer, f, k, v, false, static_cast<cudaStream_t>(stream));
@@ -986,7 +991,8 @@ la_status chunk_attention(la_cache* c, int layer, const void* q, const void* k_c
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
   if (!c->selected) return LA_ERR_STATE;
-  if (layer < 0 || layer >= g.num_layers || !q || !k_cur || !v_cur || !out)
+  if (layer < 0 || layer >= g.num_layers || !q || !k_cur || !v_cur || !out || !aligned16(q) ||
+      !aligned16(k_cur) || !aligned16(v_cur) || !aligned16(out))
     return LA_ERR_INVALID_ARG;
   if (final && c->appended[layer]) return LA_ERR_STATE;
   if (is_prsink(g) && is_external(g)) {
@@ -1112,7 +1118,8 @@ la_status la_cache_append_block(la_cache_t* c, int layer, const void* k, const v
   if (st != LA_OK) return st;
   const auto& g = c->cfg;
   if (!c->selected) return LA_ERR_STATE;
-  if (layer < 0 || layer >= g.num_layers || !k || !v) return LA_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= g.num_layers || !k || !v || !aligned16(k) || !aligned16(v))
+    return LA_ERR_INVALID_ARG;
   if (c->appended[layer]) return LA_ERR_STATE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int b = c->b;

@@ -24,7 +24,9 @@
  *     valid until that work completes.
  *   - Q/K/V/O tensors of one block are row-major [T][H][D]: T tokens in
  *     raster order (frame, row, column), H heads, D head dim; element type
- *     `q_dtype` (LA_F32 or LA_BF16).
+ *     `q_dtype` (LA_F32 or LA_BF16).  Their device pointers, and the ConvKV
+ *     weights, must be 16-byte aligned (the kernels move rows in 16-byte
+ *     vectors); a call given one that is not returns LA_ERR_INVALID_ARG.
  *   - Errors: arguments and call order are checked synchronously and the
  *     status is returned.  Faults seen inside kernels (an index out of range,
  *     a wait that ran out of time) are latched in a device error word that

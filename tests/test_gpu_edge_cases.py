@@ -96,3 +96,34 @@ def test_sixteen_slots():
         H.compare(outs[16][(0, 0)], o, "bf16", "block 16")
     else:
         assert ref[16].gap <= 1e-6
+
+
+@pytest.mark.parametrize("impl", [1, 2], ids=["tensor", "simt"])
+def test_misaligned_tensors_rejected_cache_stays_usable(impl):
+    """Q/K/V/O pointers that are not 16-byte aligned are refused before any
+    work is enqueued (the kernels move rows in 16-byte vectors), and the
+    cache goes on working with aligned ones."""
+    import torch
+    from bounded_kv_cache_la_b300 import capi
+    sc = C2_MID.with_(num_heads=2, grid_h=4, grid_w=4)
+    cache = H.make_cache(sc.with_(num_layers=1), attn_impl=impl)
+    kps = gen.poses(sc, n_blocks=2)
+    cache.la_select_context(kps[0])
+    q, k, v = H.torch_values(sc, 0, 0, 0)
+    out = torch.empty_like(q)
+    buf = torch.zeros(q.numel() + 8, dtype=q.dtype, device="cuda")
+    shifted = buf[2:2 + q.numel()].view_as(q)            # 4 bytes past a 16-byte boundary
+    shifted.copy_(q)
+    for args in ((shifted, k, v, out), (q, shifted, v, out), (q, k, shifted, out),
+                 (q, k, v, shifted)):
+        with pytest.raises(capi.LaError) as e:
+            cache.la_chunk_attention(0, *args)
+        assert e.value.status == capi.LA_ERR_INVALID_ARG
+    with pytest.raises(capi.LaError) as e:
+        cache.la_cache_append_block(0, shifted, v)
+    assert e.value.status == capi.LA_ERR_INVALID_ARG
+    cache.la_chunk_attention(0, q, k, v, out)
+    cache.la_cache_append_block(0, k, v)
+    torch.cuda.synchronize()
+    st, msg = cache.la_get_error()
+    assert st == capi.LA_OK, msg

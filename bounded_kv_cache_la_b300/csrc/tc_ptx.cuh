@@ -44,11 +44,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-// ------------------------------------------------------------------- fences
-__device__ __forceinline__ void fence_proxy_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
                                             uint32_t bar) {

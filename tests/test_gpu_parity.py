@@ -247,3 +247,25 @@ def test_history_load_rows_equal_retrieval_rows():
     got = sorted(zip(ids.cpu().numpy()[:k].tolist(), scores.cpu().numpy()[:k].tolist()))
     assert [g[0] for g in got] == ctx["dyn_ids"]
     assert [np.float32(g[1]) for g in got] == [np.float32(x) for x in ctx["dyn_scores"]]
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_head_dim_64_cuda_cores(kv):
+    """Head dim 64 with bf16 operands (bf16 or e4m3 cache) goes through the
+    CUDA-core kernel: blocks of 3 x 5 x 7 = 105 tokens (each slot ends in a
+    partial 32-key tile, the last 16-row query tile is partial), all rows
+    against the oracle, before and after the dynamic sink fills."""
+    sc = C1_TINY.with_(qkv_dtype="bf16", kv_dtype=kv, frames_per_block=3, grid_h=5, grid_w=7,
+                       num_heads=3)
+    keep = {0, 4, 6, 9}
+    _, ctxs, outs = H.run_stream(sc, 10, keep)
+    ref = ostream.plan_stream(sc, gen.poses(sc, n_blocks=10), 10)
+    vals = H.Values(sc)
+    for b in sorted(keep):
+        ctx = ref[b]
+        assert ctxs[b]["kv_len"] == ctx.kv_len
+        if ctxs[b]["dyn_ids"] != ctx.dyn_ids:
+            assert ctx.gap <= 1e-6
+            continue
+        o = H.oracle_output(sc, ctx, vals, 0, 0, 1)
+        H.compare(outs[b][(0, 0)], o, "bf16" if kv == "bf16" else "e4m3", f"block {b}")

@@ -197,13 +197,34 @@ __device__ __forceinline__ void turn_static(const QrotArgs& a, int t, int d0, co
   }
 }
 
+// The (cos, cos, sin, sin) rows the tile needs -- every slot, the one or
+// two frames its 64 tokens fall in -- are staged in shared memory first, so
+// the slot loop does not wait on table loads; pair p = 4c + e of a row sits
+// at e * 8 + c, so the 8 threads of a token read 8 consecutive entries.
 // 4 CTAs per SM (at most 64 registers) keep more Q loads in flight.
+constexpr int kStageFrames = 2;
+constexpr int kStagePairs = 32;                       // split rows: dt <= D / 2 = 64
 __global__ void __launch_bounds__(256, 4) qrot_split_kernel(QrotArgs a) {
   __shared__ int s_dq[kMaxAttnSlots];                 // t0_cur - t0_s
+  __shared__ float4 s_tab[kMaxAttnSlots][kStageFrames][kStagePairs];
   if (!slot_offsets(a, s_dq)) return;
   const int n_slots = a.ctx->n_slots;
   const int h = blockIdx.y;
-  const int ta = blockIdx.x * kSplitTokensPerCta + 2 * (threadIdx.x >> 3);
+  const int pairs_t = a.rope.dt >> 1;
+  const int t_first = blockIdx.x * kSplitTokensPerCta;
+  const int f_lo = (int)fdiv((uint32_t)t_first, a.rope.div_hw);
+  const int nf = (int)fdiv((uint32_t)min(t_first + kSplitTokensPerCta, a.T) - 1, a.rope.div_hw) - f_lo + 1;
+  const bool staged = nf <= kStageFrames && pairs_t <= kStagePairs;
+  if (staged) {
+    const int per_slot = nf * pairs_t;
+    for (int i = threadIdx.x; i < n_slots * per_slot; i += blockDim.x) {
+      const int sl = i / per_slot, rem = i - sl * per_slot;
+      const int fi = rem / pairs_t, pr = rem - fi * pairs_t;
+      s_tab[sl][fi][(pr & 3) * 8 + (pr >> 2)] = a.rope.tab_t2[(size_t)(s_dq[sl] + f_lo + fi) * pairs_t + pr];
+    }
+  }
+  __syncthreads();
+  const int ta = t_first + 2 * (threadIdx.x >> 3);
   const int tb = ta + 1;
   if (ta >= a.T) return;
   const bool has_b = tb < a.T;
@@ -234,7 +255,7 @@ __global__ void __launch_bounds__(256, 4) qrot_split_kernel(QrotArgs a) {
   turn_static(a, has_b ? tb : ta, d0, xb, yb);
   const int fa = (int)fdiv((uint32_t)ta, a.rope.div_hw);
   const int fb = has_b ? (int)fdiv((uint32_t)tb, a.rope.div_hw) : fa;
-  const int pairs_t = a.rope.dt >> 1, pair0 = d0 >> 1;
+  const int pair0 = d0 >> 1;
   const int np = min(max((a.rope.dt - d0) >> 1, 0), 4);   // temporal pairs here
   // packed (token a, token b) operands of the temporal pairs
   float2 x0[4], x1[4], nx1[4];
@@ -249,7 +270,20 @@ __global__ void __launch_bounds__(256, 4) qrot_split_kernel(QrotArgs a) {
 #pragma unroll 2
   for (int s = 0; s < n_slots; ++s, off += slot_stride) {
     if (np > 0) {
-      if (fa == fb) {
+      if (staged) {
+        const float4* ra = &s_tab[s][fa - f_lo][pair0 >> 2];
+        const float4* rb = &s_tab[s][fb - f_lo][pair0 >> 2];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e < np) {
+            const float4 ca = ra[e * 8], cb = rb[e * 8];
+            const float2 y0 = ffma2(nx1[e], make_float2(ca.z, cb.z), fmul2(x0[e], make_float2(ca.x, cb.x)));
+            const float2 y1 = ffma2(x0[e], make_float2(ca.z, cb.z), fmul2(x1[e], make_float2(ca.x, cb.x)));
+            ya[2 * e] = y0.x; yb[2 * e] = y0.y;
+            ya[2 * e + 1] = y1.x; yb[2 * e + 1] = y1.y;
+          }
+        }
+      } else if (fa == fb) {
         const float4* row = a.rope.tab_t2 + (size_t)(s_dq[s] + fa) * pairs_t + pair0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {

@@ -665,14 +665,58 @@ static int attn_tc_grid(int T, int H, int num_sms) {
   return units < num_sms ? units : num_sms;
 }
 
-// Walks the positions in snake order.  Every CTA keeps the number of half
-// units the plain order (full units first) would give it, so the work per
-// CTA is unchanged; a half unit is placed once its head's full units have
-// started, or when the CTA has no other position left for it.
+// CTA c's i-th position in the snake order the kernel walks.
+static int snake_pos(int i, int c, int G) { return i * G + ((i & 1) ? G - 1 - c : c); }
+
+// Round-aligned deal, for grids that hold a whole, even number of heads per
+// round (G = hpr * (n_full + 1/2), as 148 SMs do for 37 query tiles per
+// head): round r runs heads r*hpr .. r*hpr+hpr-1 only.  hpr/2 CTAs run that
+// round's hpr half units, two each, while the other G - hpr/2 = hpr * n_full
+// CTAs run its full units, so every head's K/V is read within one round.
+// The CTAs that take halves are those the snake order gives one position
+// more, so the work per CTA is that of dealing full units first and half
+// units last.  Returns false (and writes nothing) when the shape does not
+// fit.
+static bool attn_tc_schedule_rounds(int T, int H, int G, int* sched) {
+  const int nt = (T + kBM - 1) / kBM, n_full = nt / 2;
+  if (!(nt & 1) || n_full < 1 || (2 * G) % (2 * n_full + 1) != 0) return false;
+  const int hpr = 2 * G / (2 * n_full + 1);
+  const int n_units = attn_tc_units(T, H), q = n_units / G, rem = n_units % G;
+  if (hpr % 2 != 0 || H % hpr != 0 || H / hpr != q || 2 * rem != H) return false;
+  std::vector<int> half_cta(rem);
+  for (int k = 0; k < rem; ++k) half_cta[k] = (q & 1) ? G - 1 - k : k;
+  std::vector<std::vector<int>> list(G);
+  std::vector<char> busy(G);
+  for (int r = 0; r < q; ++r) {
+    std::fill(busy.begin(), busy.end(), 0);
+    for (int j = 0; j < hpr / 2; ++j) {
+      const int c = half_cta[r * hpr / 2 + j];
+      busy[c] = 1;
+      list[c].push_back(H * n_full + r * hpr + 2 * j);
+      list[c].push_back(H * n_full + r * hpr + 2 * j + 1);
+    }
+    int u = r * hpr * n_full;
+    for (int c = 0; c < G; ++c)
+      if (!busy[c]) list[c].push_back(u++);
+    if (u != (r + 1) * hpr * n_full) return false;
+  }
+  for (int c = 0; c < G; ++c)
+    for (int i = 0; i < (int)list[c].size(); ++i)
+      if (snake_pos(i, c, G) >= n_units) return false;
+  for (int c = 0; c < G; ++c)
+    for (int i = 0; i < (int)list[c].size(); ++i) sched[snake_pos(i, c, G)] = list[c][i];
+  return true;
+}
+
+// Otherwise: walks the positions in snake order.  Every CTA keeps the number
+// of half units the plain order (full units first) would give it, so the
+// work per CTA is unchanged; a half unit is placed once its head's full
+// units have started, or when the CTA has no other position left for it.
 void attn_tc_schedule(int T, int H, int num_sms, int* sched) {
   const int n_full = (T + kBM - 1) / kBM / 2;
   const int n_units = attn_tc_units(T, H), n_full_total = H * n_full;
   const int G = attn_tc_grid(T, H, num_sms);
+  if (attn_tc_schedule_rounds(T, H, G, sched)) return;
   std::vector<int> cta(n_units), need_half(G, 0), left(G, 0);
   for (int p = 0; p < n_units; ++p) {
     const int i = p / G, k = p - i * G;

@@ -20,6 +20,7 @@ LA_HISTORY_RESIDENT, LA_HISTORY_EXTERNAL = 0, 1
 LA_ATTN_AUTO, LA_ATTN_TENSOR, LA_ATTN_SIMT = 0, 1, 2
 LA_MAX_SLOTS, LA_MAX_TOPK = 16, 8
 LA_NOALLOC_MAX_ROWS = 65536
+LA_UNIT_REVERSED = 1 << 30
 
 DTYPES = {"f32": LA_F32, "bf16": LA_BF16, "e4m3": LA_E4M3}
 
@@ -222,7 +223,8 @@ def la_pose_topk_noalloc(table, inv_norm, query_kp, pose_row, c0, c1, k, ids_out
 
 def la_attention_schedule(T: int, H: int, num_sms: int):
     """Host only: the unit dealt at each position by the tensor-core
-    attention (list of ints)."""
+    attention (list of ints; LA_UNIT_REVERSED set on a unit that visits its
+    slots last to first)."""
     n_max = H * ((T + 255) // 256)
     buf = (ctypes.c_int32 * max(1, n_max))()
     n = load().la_attention_schedule(T, H, num_sms, buf, n_max)

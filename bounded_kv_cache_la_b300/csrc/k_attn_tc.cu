@@ -140,7 +140,9 @@ struct Wait {
 
 // Work units: full (head, tile pair) units h * n_full + p, then one half
 // unit H * n_full + h per head when the head has an odd number of query
-// tiles.  sched[position] is the unit dealt at that position.
+// tiles.  sched[position] is the unit dealt at that position, with bit 30
+// set when the unit visits its slots last to first (the softmax does not
+// depend on the order; the deal uses it to meet K/V still in L2).
 struct Units {
   int H, n_full, n_units;
   const int* sched;
@@ -155,8 +157,10 @@ struct Units {
     return i * G + ((i & 1) ? (G - 1 - c) : c);
   }
   // The unit at position pos (< n_units).
-  __device__ __forceinline__ void get(int pos, int& h, int& row0, bool& half) const {
-    const int u = __ldg(sched + pos);
+  __device__ __forceinline__ void get(int pos, int& h, int& row0, bool& half, bool& rev) const {
+    const int raw = __ldg(sched + pos);
+    rev = (raw >> 30) & 1;
+    const int u = raw & ((1 << 30) - 1);
     const int nf = H * n_full;
     if (u < nf) {
       h = u / n_full;
@@ -273,10 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int u = units.index(i);
         if (u >= units.n_units) break;
         int h, row0;
-        bool half;
-        units.get(u, h, row0, half);
+        bool half, rev;
+        units.get(u, h, row0, half, rev);
         const int n_qt = half ? 1 : 2;
-        for (int s = 0; ok && s < n_slots; ++s) {
+        for (int si = 0; ok && si < n_slots; ++si) {
+          const int s = rev ? n_slots - 1 - si : si;
           const int nt = (cx.tokens[s] + kBN - 1) / kBN;
           int krow, vrow;
           const CUtensorMap* km = kv_map(a, cx, s, 0, h, krow);
@@ -302,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
               ++qc;
               // bf16 dims 64-127: once per unit when split (the same rows for
               // every slot), else with every slot
-              if (!F8 && (!split || s == 0)) {
+              if (!F8 && (!split || si == 0)) {
                 if (!(ok = wait(ctl.q1_empty, (q1c & 1) ^ 1, 4))) break;
                 mbar_arrive_expect_tx(smem_u32(&ctl.q1_full), n_qt * Tl::kBoxBytes);
                 for (int qi = 0; qi < n_qt; ++qi)
@@ -395,14 +400,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int u = units.index(i);
         if (u >= units.n_units) break;
         int h, row0;
-        bool half;
-        units.get(u, h, row0, half);
+        bool half, rev;
+        units.get(u, h, row0, half, rev);
         int j = 0;
-        for (int s = 0; ok && s < n_slots; ++s) {
+        for (int si = 0; ok && si < n_slots; ++si) {
+          const int s = rev ? n_slots - 1 - si : si;
           const int nt = (cx.tokens[s] + kBN - 1) / kBN;
           const int qb = qc & 1;                      // this slot's query buffer
-          const bool q1_new = !F8 && (!split || s == 0);
-          const bool q1_last = !F8 && (!split || s == n_slots - 1);
+          const bool q1_new = !F8 && (!split || si == 0);
+          const bool q1_last = !F8 && (!split || si == n_slots - 1);
           for (int kt = 0; ok && kt < nt; ++kt, ++j) {
             const int ks = kc % kKSt;
             if (!(ok = wait(ctl.k_full[ks], (kc / kKSt) & 1, 11))) break;
@@ -489,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const int u = units.index(i);
       if (u >= units.n_units) break;
       int h, row0;
-      bool half;
-      units.get(u, h, row0, half);
+      bool half, rev;
+      units.get(u, h, row0, half, rev);
       if (half && qi == 1) continue;               // the tile past the head's last rows
       const int row = row0 + qi * kBM + r;
       // e4m3: true score = q_scale(row) * k_scale(slot) * S; P is stored as
@@ -504,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       }
       float m = -INFINITY, l = 0.f;
       int j = 0;
-      for (int s = 0; ok && s < n_slots; ++s) {
+      for (int si = 0; ok && si < n_slots; ++si) {
+        const int s = rev ? n_slots - 1 - si : si;
         const int tokens = cx.tokens[s];
         const int nt = (tokens + kBN - 1) / kBN;
         // e4m3: P is stored as p * r, r = v_scale(slot) / v_max <= 1, by
@@ -666,6 +673,7 @@ static int attn_tc_grid(int T, int H, int num_sms) {
 }
 
 // CTA c's i-th position in the snake order the kernel walks.
+constexpr int kUnitReversed = 1 << 30;
 static int snake_pos(int i, int c, int G) { return i * G + ((i & 1) ? G - 1 - c : c); }
 
 // Round-aligned deal, for grids that hold a whole, even number of heads per
@@ -673,10 +681,12 @@ static int snake_pos(int i, int c, int G) { return i * G + ((i & 1) ? G - 1 - c 
 // head): round r runs heads r*hpr .. r*hpr+hpr-1 only.  hpr/2 CTAs run that
 // round's hpr half units, two each, while the other G - hpr/2 = hpr * n_full
 // CTAs run its full units, so every head's K/V is read within one round.
-// The CTAs that take halves are those the snake order gives one position
-// more, so the work per CTA is that of dealing full units first and half
-// units last.  Returns false (and writes nothing) when the shape does not
-// fit.
+// The second half unit of a CTA starts when its head's full units are well
+// into the K/V, so it visits the slots last to first: it meets the slots the
+// full units read last while they are still in L2.  The CTAs that take
+// halves are those the snake order gives one position more, so the work per
+// CTA is that of dealing full units first and half units last.  Returns
+// false (and writes nothing) when the shape does not fit.
 static bool attn_tc_schedule_rounds(int T, int H, int G, int* sched) {
   const int nt = (T + kBM - 1) / kBM, n_full = nt / 2;
   if (!(nt & 1) || n_full < 1 || (2 * G) % (2 * n_full + 1) != 0) return false;
@@ -693,7 +703,7 @@ static bool attn_tc_schedule_rounds(int T, int H, int G, int* sched) {
       const int c = half_cta[r * hpr / 2 + j];
       busy[c] = 1;
       list[c].push_back(H * n_full + r * hpr + 2 * j);
-      list[c].push_back(H * n_full + r * hpr + 2 * j + 1);
+      list[c].push_back((H * n_full + r * hpr + 2 * j + 1) | kUnitReversed);
     }
     int u = r * hpr * n_full;
     for (int c = 0; c < G; ++c)

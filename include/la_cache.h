@@ -263,8 +263,11 @@ la_status la_context_plan(const la_cache_config* cfg, int block, const int32_t* 
  * numbered H * n_full + h.  out[pos] (host, `cap` entries) receives the unit
  * dealt at position pos; positions go to the SMs in snake order (SM c takes
  * positions i * G + c on even rounds i and i * G + G - 1 - c on odd ones,
- * G = min(units, num_sms)).  Returns the number of units, or -1 for bad
+ * G = min(units, num_sms)).  Bit 30 of an entry (LA_UNIT_REVERSED) marks
+ * a unit that visits its context slots last to first; the unit number is
+ * the entry without it.  Returns the number of units, or -1 for bad
  * arguments or a short buffer. */
+#define LA_UNIT_REVERSED (1 << 30)
 int la_attention_schedule(int T, int H, int num_sms, int32_t* out, int cap);
 
 /* Test access to stored pages.  Returns the device address of the page

@@ -222,11 +222,14 @@ def test_attention_schedule_balanced_and_halves_near_their_heads(lib, T, H, sms)
     each half unit in a round where its head's full units run (so it reads
     its head's K/V from L2 with them)."""
     from bounded_kv_cache_la_b300 import capi
-    sched = capi.la_attention_schedule(T, H, sms)
+    raw = capi.la_attention_schedule(T, H, sms)
+    sched = [u & ~capi.LA_UNIT_REVERSED for u in raw]
     nt = (T + 127) // 128
     n_full = nt // 2
     n_units = H * (n_full + (nt & 1))
     assert sorted(sched) == list(range(n_units))
+    # only half units visit their slots in reverse
+    assert all(u >= H * n_full for u, r in zip(sched, raw) if r != u)
     G = min(n_units, sms)
     cta = [(p % G if (p // G) % 2 == 0 else G - 1 - p % G) for p in range(n_units)]
     rnd = [p // G for p in range(n_units)]

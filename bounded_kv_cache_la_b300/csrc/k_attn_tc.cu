@@ -21,11 +21,12 @@
 // has an odd number of query tiles its last unit is a half unit (one tile).
 // Positions are dealt to the persistent CTAs in a snake order (CTA c takes
 // position i*G + c on even rounds and i*G + G-1-c on odd rounds), and a
-// table built on the host says which unit sits at each position: full units
-// in head order, and each half unit at a position of a CTA that got fewer
-// full units, in the round where its head's full units run, so that it
-// reads its head's K/V from L2 with them rather than from DRAM in a last
-// wave of its own.
+// table built on the host says which unit sits at each position, so that
+// each head's units run in the same round and read its K/V from L2 with
+// one another rather than from DRAM again: every half unit goes to a CTA
+// that got fewer full units, in its head's round, and where the grid holds
+// a whole number of heads per round, rounds are aligned to heads and a
+// CTA's second half unit visits the slots last to first.
 //
 // CTA = 12 warps, persistent:
 //   warp 0       TMA producer (K ring, V ring, per-slot Q boxes, double-buffered)

@@ -309,16 +309,17 @@ class ClockSampler:
 
 
 def kernel_code_digest():
-    """sha256 of the attention kernel's device code and of the host code that
-    deals its work units to the SMs (which decides how much K/V is read
-    again from DRAM): the text of its file before the host launchers plus the
-    schedule functions, with comments and whitespace removed (so an edited
-    comment does not retire a capture, an edited line of code does)."""
+    """sha256 of the attention kernel's device code, of the host code that
+    deals its work to the SMs (which decides how much K/V is read again from
+    DRAM) and of the merge of split query tiles: the text of its file before
+    the host launchers plus the schedule and merge code, with comments and
+    whitespace removed (so an edited comment does not retire a capture, an
+    edited line of code does)."""
     import hashlib
     import re
     src = open(os.path.join(ROOT, "bounded_kv_cache_la_b300", "csrc", "k_attn_tc.cu")).read()
     code = src[:src.index("bool attn_tc_supported")]
-    code += src[src.index("static int snake_pos"):src.index("template <bool F8>\nstatic cudaError_t launch_attn_tc_t")]
+    code += src[src.index("int attn_tc_pieces"):src.index("template <bool F8>\nstatic cudaError_t launch_attn_tc_t")]
     code = re.sub(r"/\*.*?\*/", "", code, flags=re.S)
     code = re.sub(r"//[^\n]*", "", code)
     code = re.sub(r"\s+", "", code)

@@ -20,7 +20,6 @@ LA_HISTORY_RESIDENT, LA_HISTORY_EXTERNAL = 0, 1
 LA_ATTN_AUTO, LA_ATTN_TENSOR, LA_ATTN_SIMT = 0, 1, 2
 LA_MAX_SLOTS, LA_MAX_TOPK = 16, 8
 LA_NOALLOC_MAX_ROWS = 65536
-LA_UNIT_REVERSED = 1 << 30
 
 DTYPES = {"f32": LA_F32, "bf16": LA_BF16, "e4m3": LA_E4M3}
 
@@ -135,7 +134,7 @@ def load() -> ctypes.CDLL:
         "la_status_string": (ctypes.c_char_p, [i32]),
         "la_pose_topk_noalloc": (i32, [vp, vp, i32, ctypes.POINTER(ctypes.c_float), i32, i32, i32,
                                        i32, vp, vp, vp, vp, vp]),
-        "la_attention_schedule": (i32, [i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i32]),
+        "la_attention_schedule": (i32, [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -221,16 +220,18 @@ def la_pose_topk_noalloc(table, inv_norm, query_kp, pose_row, c0, c1, k, ids_out
         "la_pose_topk_noalloc")
 
 
-def la_attention_schedule(T: int, H: int, num_sms: int):
-    """Host only: the unit dealt at each position by the tensor-core
-    attention (list of ints; LA_UNIT_REVERSED set on a unit that visits its
-    slots last to first)."""
-    n_max = H * ((T + 255) // 256)
+def la_attention_schedule(T: int, H: int, n_slots: int, num_sms: int):
+    """Host only: the tensor-core attention's work items per CTA, as a list
+    of G lists of item numbers (full units, then pieces of a split tile)."""
+    nt = (T + 127) // 128
+    n_max = 2 * (H * (nt // 2) + (H * n_slots if nt & 1 else 0)) + 1
     buf = (ctypes.c_int32 * max(1, n_max))()
-    n = load().la_attention_schedule(T, H, num_sms, buf, n_max)
-    if n < 0:
+    G = load().la_attention_schedule(T, H, n_slots, num_sms, buf, n_max)
+    if G < 0:
         raise LaError(LA_ERR_INVALID_ARG, "la_attention_schedule")
-    return list(buf[:n])
+    off = list(buf[:G + 1])
+    items = list(buf[G + 1:G + 1 + off[G]])
+    return [items[off[c]:off[c + 1]] for c in range(G)]
 
 
 def _stream_handle(stream) -> ctypes.c_void_p:

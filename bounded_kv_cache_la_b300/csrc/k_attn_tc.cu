@@ -17,16 +17,17 @@
 // slot table says which page), 128 keys x 64 dims per box, 128-byte swizzle;
 // rows past a slot's end are zero-filled by TMA and masked to -inf.
 //
-// Work units.  A unit is (head, pair of 128-row query tiles).  When a head
-// has an odd number of query tiles its last unit is a half unit (one tile).
-// Positions are dealt to the persistent CTAs in a snake order (CTA c takes
-// position i*G + c on even rounds and i*G + G-1-c on odd rounds), and a
-// table built on the host says which unit sits at each position, so that
-// each head's units run in the same round and read its K/V from L2 with
-// one another rather than from DRAM again: every half unit goes to a CTA
-// that got fewer full units, in its head's round, and where the grid holds
-// a whole number of heads per round, rounds are aligned to heads and a
-// CTA's second half unit visits the slots last to first.
+// Work.  A full unit is (head, pair of 128-row query tiles) against the
+// whole context.  When a head has an odd number of query tiles, its last
+// tile is split by context slot into pieces (the tile against one slot);
+// each piece leaves its unnormalised output, running max and sum, and a
+// small merge kernel combines them.  Dealt whole, that tile ran without a
+// partner tile to overlap with and took 0.87 of a full unit: two of them
+// on one CTA made it the slowest by 0.74 units (at 37 query tiles per head
+// on 148 SMs).  A table built on the host lists each CTA's items; they are
+// dealt by list scheduling in groups of about one round of heads (the full
+// units, then the pieces, of each group), so pieces run beside their head's
+// full units, read its K/V from L2 with them, and fill the end.
 //
 // CTA = 12 warps, persistent:
 //   warp 0       TMA producer (K ring, V ring, per-slot Q boxes, double-buffered)
@@ -139,39 +140,43 @@ struct Wait {
   }
 };
 
-// Work units: full (head, tile pair) units h * n_full + p, then one half
-// unit H * n_full + h per head when the head has an odd number of query
-// tiles.  sched[position] is the unit dealt at that position, with bit 30
-// set when the unit visits its slots last to first (the softmax does not
-// depend on the order; the deal uses it to meet K/V still in L2).
+// Work items.  Full units h * n_full + p: query tiles 2p, 2p+1 of head h
+// against the whole context.  When a head has an odd number of query tiles,
+// its last tile is split by context slot instead: piece H * n_full + h * P + s
+// is that tile against slot s only (P = pieces per head, the most slots a
+// context can have; pieces past the context's slots are empty).  A piece
+// leaves its unnormalised output, running max and sum in `part`, and
+// attn_merge_kernel combines the pieces.  sched holds the items of each CTA:
+// sched[c] .. sched[c + 1] index the entries after the G + 1 offsets.
 struct Units {
-  int H, n_full, n_units;
-  const int* sched;
-  __device__ Units(int T, int H_, const int* sched_) : H(H_), sched(sched_) {
+  int H, n_full, n_pieces, n_full_total;
+  int begin, end;                   // this CTA's entries
+  const int* items;
+  __device__ Units(int T, int H_, int n_pieces_, const int* sched) : H(H_), n_pieces(n_pieces_) {
     const int nt_q = (T + kBM - 1) / kBM;
     n_full = nt_q / 2;
-    n_units = H * n_full + ((nt_q & 1) ? H : 0);
+    n_full_total = H * n_full;
+    begin = __ldg(sched + blockIdx.x);
+    end = __ldg(sched + blockIdx.x + 1);
+    items = sched + gridDim.x + 1;
   }
-  // CTA c's i-th position in snake order (may be >= n_units: done).
-  __device__ __forceinline__ int index(int i) const {
-    const int G = gridDim.x, c = blockIdx.x;
-    return i * G + ((i & 1) ? (G - 1 - c) : c);
-  }
-  // The unit at position pos (< n_units).
-  __device__ __forceinline__ void get(int pos, int& h, int& row0, bool& half, bool& rev) const {
-    const int raw = __ldg(sched + pos);
-    rev = (raw >> 30) & 1;
-    const int u = raw & ((1 << 30) - 1);
-    const int nf = H * n_full;
-    if (u < nf) {
+  // false when the CTA has no i-th item
+  __device__ __forceinline__ bool get(int i, int& h, int& row0, bool& piece, int& slot) const {
+    if (begin + i >= end) return false;
+    const int u = __ldg(items + begin + i);
+    if (u < n_full_total) {
       h = u / n_full;
       row0 = (u - h * n_full) * 2 * kBM;
-      half = false;
+      piece = false;
+      slot = -1;
     } else {
-      h = u - nf;
+      const int p = u - n_full_total;
+      h = p / n_pieces;
+      slot = p - h * n_pieces;
       row0 = n_full * 2 * kBM;
-      half = true;
+      piece = true;
     }
+    return true;
   }
 };
 
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const Wait wait{&ctl.abort_flag, a.err, a.timeout_ns};
   const uint64_t limit_ns = a.timeout_ns;
   const uint32_t tmem = ctl.tmem_base;
-  const Units units(a.T, a.H, a.sched);
+  const Units units(a.T, a.H, a.n_pieces, a.sched);
   if (bad && tid == 0) record_error(a.err, LA_ERR_DEVICE, KID_ATTN_TC, n_slots, -1);
 
   if (warp < 4) {
@@ -275,14 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       bool ok = true;
       const bool split = a.q_shared_z >= 0;
       for (int i = 0; ok; ++i) {
-        const int u = units.index(i);
-        if (u >= units.n_units) break;
-        int h, row0;
-        bool half, rev;
-        units.get(u, h, row0, half, rev);
-        const int n_qt = half ? 1 : 2;
-        for (int si = 0; ok && si < n_slots; ++si) {
-          const int s = rev ? n_slots - 1 - si : si;
+        int h, row0, slot;
+        bool piece;
+        if (!units.get(i, h, row0, piece, slot)) break;
+        if (piece && slot >= n_slots) continue;     // past this context's slots
+        const int n_qt = piece ? 1 : 2;
+        const int s_begin = piece ? slot : 0, s_end = piece ? slot + 1 : n_slots;
+        for (int s = s_begin; ok && s < s_end; ++s) {
           const int nt = (cx.tokens[s] + kBN - 1) / kBN;
           int krow, vrow;
           const CUtensorMap* km = kv_map(a, cx, s, 0, h, krow);
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
               ++qc;
               // bf16 dims 64-127: once per unit when split (the same rows for
               // every slot), else with every slot
-              if (!F8 && (!split || si == 0)) {
+              if (!F8 && (!split || s == s_begin)) {
                 if (!(ok = wait(ctl.q1_empty, (q1c & 1) ^ 1, 4))) break;
                 mbar_arrive_expect_tx(smem_u32(&ctl.q1_full), n_qt * Tl::kBoxBytes);
                 for (int qi = 0; qi < n_qt; ++qi)
@@ -398,18 +402,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
       };
       for (int i = 0; ok; ++i) {
-        const int u = units.index(i);
-        if (u >= units.n_units) break;
-        int h, row0;
-        bool half, rev;
-        units.get(u, h, row0, half, rev);
+        int h, row0, slot;
+        bool half;
+        if (!units.get(i, h, row0, half, slot)) break;
+        if (half && slot >= n_slots) continue;      // past this context's slots
+        const int s_begin = half ? slot : 0, s_end = half ? slot + 1 : n_slots;
         int j = 0;
-        for (int si = 0; ok && si < n_slots; ++si) {
-          const int s = rev ? n_slots - 1 - si : si;
+        for (int s = s_begin; ok && s < s_end; ++s) {
           const int nt = (cx.tokens[s] + kBN - 1) / kBN;
           const int qb = qc & 1;                      // this slot's query buffer
-          const bool q1_new = !F8 && (!split || si == 0);
-          const bool q1_last = !F8 && (!split || si == n_slots - 1);
+          const bool q1_new = !F8 && (!split || s == s_begin);
+          const bool q1_last = !F8 && (!split || s == s_end - 1);
           for (int kt = 0; ok && kt < nt; ++kt, ++j) {
             const int ks = kc % kKSt;
             if (!(ok = wait(ctl.k_full[ks], (kc / kKSt) & 1, 11))) break;
@@ -493,12 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     uint32_t sph = 0, oph = 0;
     bool ok = true;
     for (int i = 0; ok; ++i) {
-      const int u = units.index(i);
-      if (u >= units.n_units) break;
-      int h, row0;
-      bool half, rev;
-      units.get(u, h, row0, half, rev);
-      if (half && qi == 1) continue;               // the tile past the head's last rows
+      int h, row0, slot;
+      bool half;
+      if (!units.get(i, h, row0, half, slot)) break;
+      if (half && (qi == 1 || slot >= n_slots)) continue;   // one tile; past the context
+      const int s_begin = half ? slot : 0, s_end = half ? slot + 1 : n_slots;
       const int row = row0 + qi * kBM + r;
       // e4m3: true score = q_scale(row) * k_scale(slot) * S; P is stored as
       // p * v_scale(slot) / v_max so that O = v_max * sum(P V codes).
@@ -511,8 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       }
       float m = -INFINITY, l = 0.f;
       int j = 0;
-      for (int si = 0; ok && si < n_slots; ++si) {
-        const int s = rev ? n_slots - 1 - si : si;
+      for (int s = s_begin; ok && s < s_end; ++s) {
         const int tokens = cx.tokens[s];
         const int nt = (tokens + kBN - 1) / kBN;
         // e4m3: P is stored as p * r, r = v_scale(slot) / v_max <= 1, by
@@ -630,6 +631,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       if (!ok) break;
       ++oph;
       tc_fence_after();
+      if (half) {
+        // a piece: v_max * O (unnormalised, fp32), the running max and sum
+        const size_t pi = (size_t)h * a.n_pieces + slot;
+        float* po = a.part_o + (pi * kBM + r) * kD;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc * 32, o);
+          tmem_wait_ld();
+          float4* d4 = reinterpret_cast<float4*>(po + cc * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            d4[e] = make_float4(__uint_as_float(o[4 * e]) * v_max, __uint_as_float(o[4 * e + 1]) * v_max,
+                                __uint_as_float(o[4 * e + 2]) * v_max, __uint_as_float(o[4 * e + 3]) * v_max);
+        }
+        a.part_ml[pi * kBM + r] = make_float2(m, l);
+        tc_fence_before();
+        continue;
+      }
       const float inv_l = v_max / l;
       uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + ((size_t)row * a.H + h) * kD;
 #pragma unroll
@@ -666,87 +686,101 @@ bool attn_tc_supported(int D, int kv_dtype) {
   return D == kD && (kv_dtype == LA_BF16 || kv_dtype == LA_E4M3);
 }
 
-int attn_tc_units(int T, int H) { return H * ((T + 2 * kBM - 1) / (2 * kBM)); }
+int attn_tc_pieces(int T, int n_slots_max) { return ((T + kBM - 1) / kBM) & 1 ? n_slots_max : 0; }
 
-static int attn_tc_grid(int T, int H, int num_sms) {
-  const int units = attn_tc_units(T, H);
-  return units < num_sms ? units : num_sms;
+int attn_tc_items(int T, int H, int n_pieces) {
+  const int nt = (T + kBM - 1) / kBM;
+  return H * (nt / 2) + ((nt & 1) ? H * n_pieces : 0);
 }
 
-// CTA c's i-th position in the snake order the kernel walks.
-constexpr int kUnitReversed = 1 << 30;
-static int snake_pos(int i, int c, int G) { return i * G + ((i & 1) ? G - 1 - c : c); }
+size_t attn_tc_sched_ints(int T, int H, int n_pieces) { return 2 * (size_t)attn_tc_items(T, H, n_pieces) + 1; }
 
-// Round-aligned deal, for grids that hold a whole, even number of heads per
-// round (G = hpr * (n_full + 1/2), as 148 SMs do for 37 query tiles per
-// head): round r runs heads r*hpr .. r*hpr+hpr-1 only.  hpr/2 CTAs run that
-// round's hpr half units, two each, while the other G - hpr/2 = hpr * n_full
-// CTAs run its full units, so every head's K/V is read within one round.
-// The second half unit of a CTA starts when its head's full units are well
-// into the K/V, so it visits the slots last to first: it meets the slots the
-// full units read last while they are still in L2.  The CTAs that take
-// halves are those the snake order gives one position more, so the work per
-// CTA is that of dealing full units first and half units last.  Returns
-// false (and writes nothing) when the shape does not fit.
-static bool attn_tc_schedule_rounds(int T, int H, int G, int* sched) {
+// List scheduling.  Items go, in order, to the CTA that is free first (by
+// estimated time: a full unit 1, a piece the tile's share of a context slot,
+// 0.87 / P -- one query tile without a partner takes 0.87 of a two-tile
+// unit -- plus 0.02 for its start and end).  The order takes heads in
+// groups of about one round (G / (n_full + 1/2) heads): a group's full units,
+// then its pieces, so the pieces run beside their head's full units and read
+// its K/V from L2 with them, and the short pieces fill the time the full
+// units leave at the end.  Returns the grid G; out receives G + 1 offsets,
+// then the items of CTA 0, CTA 1, ...
+int attn_tc_schedule(int T, int H, int n_pieces, int num_sms, int* out) {
   const int nt = (T + kBM - 1) / kBM, n_full = nt / 2;
-  if (!(nt & 1) || n_full < 1 || (2 * G) % (2 * n_full + 1) != 0) return false;
-  const int hpr = 2 * G / (2 * n_full + 1);
-  const int n_units = attn_tc_units(T, H), q = n_units / G, rem = n_units % G;
-  if (hpr % 2 != 0 || H % hpr != 0 || H / hpr != q || 2 * rem != H) return false;
-  std::vector<int> half_cta(rem);
-  for (int k = 0; k < rem; ++k) half_cta[k] = (q & 1) ? G - 1 - k : k;
+  const int P = (nt & 1) ? n_pieces : 0;
+  const int n_items = attn_tc_items(T, H, n_pieces);
+  const int G = n_items < num_sms ? n_items : num_sms;
+  const int per_round = std::max(1, (int)(2.0 * G / (2 * n_full + 1) + 0.5));
+  const double t_full = 1.0, t_piece = P > 0 ? 0.87 / P + 0.02 : 0.0;
   std::vector<std::vector<int>> list(G);
-  std::vector<char> busy(G);
-  for (int r = 0; r < q; ++r) {
-    std::fill(busy.begin(), busy.end(), 0);
-    for (int j = 0; j < hpr / 2; ++j) {
-      const int c = half_cta[r * hpr / 2 + j];
-      busy[c] = 1;
-      list[c].push_back(H * n_full + r * hpr + 2 * j);
-      list[c].push_back((H * n_full + r * hpr + 2 * j + 1) | kUnitReversed);
-    }
-    int u = r * hpr * n_full;
-    for (int c = 0; c < G; ++c)
-      if (!busy[c]) list[c].push_back(u++);
-    if (u != (r + 1) * hpr * n_full) return false;
+  std::vector<std::pair<double, int>> heap;
+  for (int c = G - 1; c >= 0; --c) heap.emplace_back(0.0, c);
+  auto cmp = [](const std::pair<double, int>& x, const std::pair<double, int>& y) {
+    return x.first > y.first || (x.first == y.first && x.second > y.second);
+  };
+  std::make_heap(heap.begin(), heap.end(), cmp);
+  auto deal = [&](int item, double t) {
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    auto& top = heap.back();
+    list[top.second].push_back(item);
+    top.first += t;
+    std::push_heap(heap.begin(), heap.end(), cmp);
+  };
+  for (int h0 = 0; h0 < H; h0 += per_round) {
+    const int h1 = std::min(H, h0 + per_round);
+    for (int h = h0; h < h1; ++h)
+      for (int p = 0; p < n_full; ++p) deal(h * n_full + p, t_full);
+    for (int h = h0; h < h1; ++h)
+      for (int sl = 0; sl < P; ++sl) deal(H * n_full + h * P + sl, t_piece);
   }
-  for (int c = 0; c < G; ++c)
-    for (int i = 0; i < (int)list[c].size(); ++i)
-      if (snake_pos(i, c, G) >= n_units) return false;
-  for (int c = 0; c < G; ++c)
-    for (int i = 0; i < (int)list[c].size(); ++i) sched[snake_pos(i, c, G)] = list[c][i];
-  return true;
+  int k = 0;
+  for (int c = 0; c < G; ++c) {
+    out[c] = k;
+    for (int u : list[c]) out[G + 1 + k++] = u;
+  }
+  out[G] = k;
+  return G;
 }
 
-// Otherwise: walks the positions in snake order.  Every CTA keeps the number
-// of half units the plain order (full units first) would give it, so the
-// work per CTA is unchanged; a half unit is placed once its head's full
-// units have started, or when the CTA has no other position left for it.
-void attn_tc_schedule(int T, int H, int num_sms, int* sched) {
-  const int n_full = (T + kBM - 1) / kBM / 2;
-  const int n_units = attn_tc_units(T, H), n_full_total = H * n_full;
-  const int G = attn_tc_grid(T, H, num_sms);
-  if (attn_tc_schedule_rounds(T, H, G, sched)) return;
-  std::vector<int> cta(n_units), need_half(G, 0), left(G, 0);
-  for (int p = 0; p < n_units; ++p) {
-    const int i = p / G, k = p - i * G;
-    cta[p] = (i & 1) ? G - 1 - k : k;
-    ++left[cta[p]];
-    if (p >= n_full_total) ++need_half[cta[p]];
+// Merge of a split query tile: for each of its rows and head, the pieces'
+// outputs O_s (times v_max), running maxima m_s and sums l_s combine as
+//   O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s.
+// One warp per row, 4 dims per lane.
+__global__ void __launch_bounds__(128) attn_merge_kernel(const MergeArgs a) {
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5);          // row within the tile
+  const int h = blockIdx.y, lane = threadIdx.x & 31;
+  const int row = a.row0 + r;
+  if (row >= a.T) return;
+  const int n = a.ctx->n_slots;
+  if (n < 1 || n > a.n_pieces) {
+    if (lane == 0 && r == 0 && h == 0) record_error(a.err, LA_ERR_DEVICE, KID_ATTN_TC, n, a.n_pieces);
+    return;
   }
-  int fi = 0, hi = 0;
-  for (int p = 0; p < n_units; ++p) {
-    const int c = cta[p];
-    const int heads_started = n_full > 0 ? std::min(H, (fi + n_full - 1) / n_full) : H;
-    if (need_half[c] > 0 && (left[c] == need_half[c] || hi < heads_started)) {
-      sched[p] = n_full_total + hi++;
-      --need_half[c];
-    } else {
-      sched[p] = fi++;
-    }
-    --left[c];
+  const size_t base = (size_t)h * a.n_pieces;
+  float M = -INFINITY;
+  for (int sl = 0; sl < n; ++sl) M = fmaxf(M, a.part_ml[(base + sl) * kBM + r].x);
+  float den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sl = 0; sl < n; ++sl) {
+    const float2 ml = a.part_ml[(base + sl) * kBM + r];
+    const float w = exp2f(ml.x - M);
+    den += w * ml.y;
+    const float4 o = reinterpret_cast<const float4*>(a.part_o + ((base + sl) * kBM + r) * kD)[lane];
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
   }
+  const float inv = 1.f / den;
+  uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + ((size_t)row * a.H + h) * kD + lane * 4;
+  *reinterpret_cast<uint2*>(dst) = make_uint2(cvt_bf16x2(acc.x * inv, acc.y * inv), cvt_bf16x2(acc.z * inv, acc.w * inv));
+}
+
+cudaError_t launch_attn_merge(const MergeArgs& a, cudaStream_t s) {
+  if (a.n_pieces < 1 || a.T < 1 || a.H < 1 || a.H > 65535 || a.row0 >= a.T) return cudaErrorInvalidValue;
+  const int rows = std::min(kBM, a.T - a.row0);
+  attn_merge_kernel<<<dim3((rows + 3) / 4, a.H), 128, 0, s>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 template <bool F8>
@@ -763,8 +797,8 @@ static cudaError_t launch_attn_tc_t(const TcAttnArgs& a, int num_sms, cudaStream
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int grid = attn_tc_grid(a.T, a.H, num_sms);
-  attn_tc_kernel<F8><<<grid, kThreads, Tile<F8>::kSmem, s>>>(a);
+  (void)num_sms;
+  attn_tc_kernel<F8><<<a.grid, kThreads, Tile<F8>::kSmem, s>>>(a);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -58,7 +58,9 @@ struct la_cache {
   bool tc = false;
   bool q_split = false;          // split rotated-query layout (see QrotArgs)
   CUtensorMap tm_q{}, tm_kv{}, tm_cur{}, tm_mem{};
-  std::vector<int> sched;           // tensor path: unit at each dealt position (uploaded)
+  std::vector<int> sched;           // tensor path: work items per CTA (uploaded)
+  int attn_grid = 0;                // tensor path: CTAs of the attention launch
+  int n_pieces = 0;                 // tensor path: pieces per head of a split query tile
   int num_sms = 148;
   std::vector<cudaEvent_t> prof_start, prof_stop;
   int inject_stall = 0;             // tensor-core launches still to stall (tests)
@@ -193,7 +195,10 @@ void compute_layout(const la_cache_config& c, Layout& L) {
   const bool f8 = c.kv_dtype == LA_E4M3;
   L.qrot = take(tc ? (size_t)L.n_qrot * H * T * D * (f8 ? 1 : 2) : 0);
   L.qscale = take(tc && f8 ? sizeof(float) * (size_t)H * T : 0);
-  L.sched = take(tc ? sizeof(int) * (size_t)attn_tc_units(T, H) : 0);
+  const int n_pieces = tc ? attn_tc_pieces(T, L.n_qrot) : 0;
+  L.sched = take(tc ? sizeof(int) * attn_tc_sched_ints(T, H, n_pieces) : 0);
+  L.part_o = take(sizeof(float) * (size_t)H * n_pieces * 128 * D);
+  L.part_ml = take(sizeof(float2) * (size_t)H * n_pieces * 128);
   L.rope_t2 = take(tc && !f8 ? sizeof(float4) * (size_t)L.max_t * (c.rope_t / 2 > 0 ? c.rope_t / 2 : 1) : 0);
   L.mem = take(is_prsink(c) ? 0 : (size_t)c.num_layers * 3 * H * c.mem_slots * D * 2);
   L.total = off;
@@ -508,14 +513,17 @@ la_status la_context_plan(const la_cache_config* cfg, int block, const int32_t* 
   return LA_OK;
 }
 
-int la_attention_schedule(int T, int H, int num_sms, int32_t* out, int cap) {
-  if (T < 1 || T > kMaxBlockTokens || H < 1 || H > 64 || num_sms < 1 || !out) return -1;
-  const int n = attn_tc_units(T, H);
+int la_attention_schedule(int T, int H, int n_slots, int num_sms, int32_t* out, int cap) {
+  if (T < 1 || T > kMaxBlockTokens || H < 1 || H > 64 || n_slots < 1 || n_slots > kMaxAttnSlots ||
+      num_sms < 1 || !out)
+    return -1;
+  const int n_pieces = attn_tc_pieces(T, n_slots);
+  std::vector<int> sched(attn_tc_sched_ints(T, H, n_pieces));
+  const int G = attn_tc_schedule(T, H, n_pieces, num_sms, sched.data());
+  const int n = G + 1 + sched[G];
   if (cap < n) return -1;
-  std::vector<int> sched((size_t)n);
-  attn_tc_schedule(T, H, num_sms, sched.data());
   for (int i = 0; i < n; ++i) out[i] = sched[i];
-  return n;
+  return G;
 }
 
 // Builds the cache object over the caller's pool; init_pool: zero the
@@ -611,10 +619,12 @@ static la_status create_cache(const la_cache_config* cfg, void* dev_pool, size_t
     // the work-unit table depends on this device's SM count: built on every
     // create, a restored pool included
     if (st == LA_OK) {
-      c->sched.resize((size_t)attn_tc_units(c->T, H));
-      attn_tc_schedule(c->T, H, c->num_sms, c->sched.data());
-      st = cuda_status(c, cudaMemcpyAsync(c->pool + L.sched, c->sched.data(),
-                                          sizeof(int) * c->sched.size(), cudaMemcpyHostToDevice, s),
+      c->n_pieces = attn_tc_pieces(c->T, L.n_qrot);
+      c->sched.assign(attn_tc_sched_ints(c->T, H, c->n_pieces), 0);
+      c->attn_grid = attn_tc_schedule(c->T, H, c->n_pieces, c->num_sms, c->sched.data());
+      const size_t n_ints = (size_t)c->attn_grid + 1 + c->sched[c->attn_grid];
+      st = cuda_status(c, cudaMemcpyAsync(c->pool + L.sched, c->sched.data(), sizeof(int) * n_ints,
+                                          cudaMemcpyHostToDevice, s),
                        "upload work-unit table");
     }
   }
@@ -1048,6 +1058,10 @@ la_status chunk_attention(la_cache* c, int layer, const void* q, const void* k_c
     ta.tm_mem = c->tm_mem;
     ta.ctx = dctx;
     ta.sched = reinterpret_cast<const int*>(c->pool + c->L.sched);
+    ta.grid = c->attn_grid;
+    ta.n_pieces = c->n_pieces;
+    ta.part_o = reinterpret_cast<float*>(c->pool + c->L.part_o);
+    ta.part_ml = reinterpret_cast<float2*>(c->pool + c->L.part_ml);
     ta.kv_f8 = g.kv_dtype == LA_E4M3;
     ta.q_shared_z = c->q_split ? c->L.n_qrot * g.num_heads : -1;
     ta.frame_scales = ta.kv_f8 ? frame_scales(c, layer, 0) : nullptr;
@@ -1068,6 +1082,20 @@ la_status chunk_attention(la_cache* c, int layer, const void* q, const void* k_c
     const bool prof = c->prof_next < c->prof_start.size();
     if (prof) cudaEventRecord(c->prof_start[c->prof_next], s);
     st = cuda_status(c, launch_attn_tc(ta, c->num_sms, s), "tensor-core attention");
+    if (st == LA_OK && c->n_pieces > 0) {
+      // the last query tile, split by slot: combine its pieces
+      MergeArgs ma{};
+      ma.ctx = dctx;
+      ma.part_o = ta.part_o;
+      ma.part_ml = ta.part_ml;
+      ma.out = out;
+      ma.T = c->T;
+      ma.H = g.num_heads;
+      ma.row0 = (c->T / 256) * 256;
+      ma.n_pieces = c->n_pieces;
+      ma.err = err;
+      st = cuda_status(c, launch_attn_merge(ma, s), "attention merge");
+    }
     if (prof) cudaEventRecord(c->prof_stop[c->prof_next++], s);
     return st;
   }

@@ -67,7 +67,8 @@ struct Layout {
   size_t rope_t2;                  // bf16 tensor path: temporal table as (cos, cos, sin, sin)
   size_t ctx_inject;               // slot table of an injected failure (la_debug_inject)
   size_t qscale;                   // e4m3 tensor path: [H][T] fp32 query scales
-  size_t sched;                    // tensor path: [work units] unit at each dealt position
+  size_t sched;                    // tensor path: work items per CTA (attn_tc_schedule)
+  size_t part_o, part_ml;          // tensor path, odd query-tile count: pieces' partial results
   size_t mem;                      // ConvKV [L][3][H][cap][D] bf16 (raw K, V, rotated K)
   size_t total;
   size_t page_bytes;               // H * T * D * elt(kv_dtype)
@@ -205,8 +206,11 @@ struct TcAttnArgs {
   CUtensorMap tm_cur;  // current pages    [2*H][T][D]
   CUtensorMap tm_mem;  // ConvKV rings     [L*3*H][cap][D] (or a dummy)
   const DevContext* ctx;
-  const int* sched;           // [H * ceil(T / 256)] unit dealt at each position
-                              // (attn_tc_schedule for the launch's grid)
+  const int* sched;           // work items per CTA (attn_tc_schedule for `grid`)
+  int grid;                   // CTAs (attn_tc_schedule's return value)
+  int n_pieces;               // pieces per head of a split query tile (0: none)
+  float* part_o;              // pieces: [H][n_pieces][128][D] fp32, v_max * O unnormalised
+  float2* part_ml;            // pieces: [H][n_pieces][128] (running max, sum)
   const float* frame_scales;  // e4m3: this layer's [n_frames][2][H]
   const float* cur_scales;    // e4m3: [2][H]
   const float* q_scales;      // e4m3: [H][T]
@@ -226,10 +230,27 @@ struct TcAttnArgs {
   DevError* err;
 };
 cudaError_t launch_attn_tc(const TcAttnArgs& a, int num_sms, cudaStream_t s);
-// Work units and the table of the unit dealt at each position, for the grid
-// launch_attn_tc uses with num_sms SMs.
-int attn_tc_units(int T, int H);
-void attn_tc_schedule(int T, int H, int num_sms, int* sched);
+// Work items of the tensor-core attention: full units (two query tiles) and,
+// when a head has an odd number of query tiles, n_pieces pieces per head of
+// its last tile (one per context slot; n_pieces = the most slots a context
+// has, attn_tc_pieces gives 0 when there is no odd tile).
+int attn_tc_pieces(int T, int n_slots_max);
+int attn_tc_items(int T, int H, int n_pieces);
+size_t attn_tc_sched_ints(int T, int H, int n_pieces);   // bound of the table's size
+// Deals the items to at most num_sms CTAs; returns the grid G and fills out
+// with G + 1 offsets followed by each CTA's items.
+int attn_tc_schedule(int T, int H, int n_pieces, int num_sms, int* out);
 bool attn_tc_supported(int D, int kv_dtype);
+
+// Combines the pieces of the split query tile into rows row0 .. T-1 of out.
+struct MergeArgs {
+  const DevContext* ctx;      // n_slots: pieces that hold results
+  const float* part_o;
+  const float2* part_ml;
+  void* out;                  // [T][H][D] bf16
+  int T, H, row0, n_pieces;
+  DevError* err;
+};
+cudaError_t launch_attn_merge(const MergeArgs& a, cudaStream_t s);
 
 }  // namespace la

@@ -257,18 +257,17 @@ la_status la_context_plan(const la_cache_config* cfg, int block, const int32_t* 
                           int n_dyn, la_context* out);
 
 /* Host only, no device work: how the tensor-core attention deals its work
- * units to a device with `num_sms` SMs, for blocks of T tokens and H heads.
- * A unit is (head, pair of 128-row query tiles), numbered h * n_full + p;
- * a head with an odd number of query tiles adds a half unit (one tile),
- * numbered H * n_full + h.  out[pos] (host, `cap` entries) receives the unit
- * dealt at position pos; positions go to the SMs in snake order (SM c takes
- * positions i * G + c on even rounds i and i * G + G - 1 - c on odd ones,
- * G = min(units, num_sms)).  Bit 30 of an entry (LA_UNIT_REVERSED) marks
- * a unit that visits its context slots last to first; the unit number is
- * the entry without it.  Returns the number of units, or -1 for bad
- * arguments or a short buffer. */
-#define LA_UNIT_REVERSED (1 << 30)
-int la_attention_schedule(int T, int H, int num_sms, int32_t* out, int cap);
+ * to a device with `num_sms` SMs, for blocks of T tokens, H heads and
+ * contexts of at most n_slots slots.  Items: full units (h, p), numbered
+ * h * n_full + p, each query tiles 2p and 2p+1 of head h (128 rows each)
+ * against the whole context; when a head has an odd number of query tiles,
+ * its last tile goes in pieces, one per slot, numbered
+ * H * n_full + h * n_slots + s (the tile against slot s alone; a separate
+ * pass merges the pieces).  out (host, `cap` entries) receives G + 1
+ * offsets, then the items of CTA 0, CTA 1, ...: CTA c runs entries
+ * out[G + 1 + out[c]] .. out[G + 1 + out[c + 1] - 1] in order.  Returns the
+ * grid G, or -1 for bad arguments or a short buffer. */
+int la_attention_schedule(int T, int H, int n_slots, int num_sms, int32_t* out, int cap);
 
 /* Test access to stored pages.  Returns the device address of the page
  * holding `which` (0 = RoPE'd key, 1 = value, 2 = raw key [ConvKV]) of

@@ -213,40 +213,44 @@ int main() {
     assert out.returncode == 0 and bad == 0 and checked == 5000 * 4004
 
 
-@pytest.mark.parametrize("T,H,sms", [(4680, 40, 148), (3510, 40, 148), (1560, 12, 148),
-                                     (48, 3, 148), (4680, 64, 148), (4680, 40, 132),
-                                     (390, 4, 148), (4680, 1, 148)])
-def test_attention_schedule_balanced_and_halves_near_their_heads(lib, T, H, sms):
-    """The tensor-core attention's work-unit table: every unit once, the
-    same work per SM as dealing full units first and half units last, and
-    each half unit in a round where its head's full units run (so it reads
-    its head's K/V from L2 with them)."""
+@pytest.mark.parametrize("T,H,S,sms", [(4680, 40, 7, 148), (4680, 40, 9, 148), (4680, 40, 5, 148),
+                                       (3510, 40, 7, 148), (1560, 12, 6, 148), (48, 3, 4, 148),
+                                       (4680, 64, 7, 148), (4680, 40, 7, 132), (390, 4, 6, 148),
+                                       (4680, 1, 7, 148), (4608, 40, 7, 148)])
+def test_attention_schedule_every_item_once_and_balanced(lib, T, H, S, sms):
+    """The tensor-core attention's work table: every item exactly once, at
+    most num_sms CTAs, the estimated time per CTA within one item of the
+    mean (list scheduling), each piece of a split tile dealt after its
+    head's full units, and at the 14B shape (37 query tiles per head) a
+    slowest CTA under 5.3 full units (dealing the odd tile whole, two per
+    CTA on 20 CTAs, gave 5.74)."""
     from bounded_kv_cache_la_b300 import capi
-    raw = capi.la_attention_schedule(T, H, sms)
-    sched = [u & ~capi.LA_UNIT_REVERSED for u in raw]
+    lists = capi.la_attention_schedule(T, H, S, sms)
     nt = (T + 127) // 128
     n_full = nt // 2
-    n_units = H * (n_full + (nt & 1))
-    assert sorted(sched) == list(range(n_units))
-    # only half units visit their slots in reverse
-    assert all(u >= H * n_full for u, r in zip(sched, raw) if r != u)
-    G = min(n_units, sms)
-    cta = [(p % G if (p // G) % 2 == 0 else G - 1 - p % G) for p in range(n_units)]
-    rnd = [p // G for p in range(n_units)]
-    work = lambda u: 1.0 if u < H * n_full else 0.5
-    load, plain = [0.0] * G, [0.0] * G
-    for p, u in enumerate(sched):
-        load[cta[p]] += work(u)
-        plain[cta[p]] += work(p)
-    assert load == plain
-    full_rounds = {}
-    for p, u in enumerate(sched):
-        if u < H * n_full:
-            full_rounds.setdefault(u // n_full, []).append(rnd[p])
-    for p, u in enumerate(sched):
-        if u >= H * n_full and n_full > 0:
-            rs = full_rounds[u - H * n_full]
-            assert min(rs) - 1 <= rnd[p] <= max(rs) + 1, (u, rnd[p], rs)
+    P = S if nt & 1 else 0
+    n_items = H * n_full + H * P
+    G = min(n_items, sms)
+    assert len(lists) == G
+    assert sorted(u for l in lists for u in l) == list(range(n_items))
+    t_piece = 0.87 / P + 0.02 if P else 0.0
+    cost = lambda u: 1.0 if u < H * n_full else t_piece
+    load = [sum(cost(u) for u in l) for l in lists]
+    assert max(load) <= sum(load) / G + 1.0 + 1e-9
+    order = {}
+    for c, l in enumerate(lists):
+        for i, u in enumerate(l):
+            order[u] = (c, i)
+    if T == 4680 and H == 40 and sms == 148:
+        assert max(load) < 5.3
+    # the pieces of a head never run before one of its full units on the same CTA
+    for c, l in enumerate(lists):
+        seen_piece_heads = set()
+        for u in l:
+            if u >= H * n_full:
+                seen_piece_heads.add((u - H * n_full) // P)
+            else:
+                assert u // n_full not in seen_piece_heads
     assert capi.la_attention_schedule.__doc__
     with pytest.raises(capi.LaError):
-        capi.la_attention_schedule(0, H, sms)
+        capi.la_attention_schedule(0, H, S, sms)

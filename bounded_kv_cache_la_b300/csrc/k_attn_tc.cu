@@ -696,9 +696,9 @@ int attn_tc_items(int T, int H, int n_pieces) {
 size_t attn_tc_sched_ints(int T, int H, int n_pieces) { return 2 * (size_t)attn_tc_items(T, H, n_pieces) + 1; }
 
 // List scheduling.  Items go, in order, to the CTA that is free first (by
-// estimated time: a full unit 1, a piece the tile's share of a context slot,
-// 0.87 / P -- one query tile without a partner takes 0.87 of a two-tile
-// unit -- plus 0.02 for its start and end).  The order takes heads in
+// estimated time: a full unit 1, a piece 0.78 / P + 0.02 -- timestamps at
+// 37 query tiles per head gave 0.129 of a full unit for each of 7 pieces
+// and 0.106 for each of 9).  The order takes heads in
 // groups of about one round (G / (n_full + 1/2) heads): a group's full units,
 // then its pieces, so the pieces run beside their head's full units and read
 // its K/V from L2 with them, and the short pieces fill the time the full
@@ -710,7 +710,7 @@ int attn_tc_schedule(int T, int H, int n_pieces, int num_sms, int* out) {
   const int n_items = attn_tc_items(T, H, n_pieces);
   const int G = n_items < num_sms ? n_items : num_sms;
   const int per_round = std::max(1, (int)(2.0 * G / (2 * n_full + 1) + 0.5));
-  const double t_full = 1.0, t_piece = P > 0 ? 0.87 / P + 0.02 : 0.0;
+  const double t_full = 1.0, t_piece = P > 0 ? 0.78 / P + 0.02 : 0.0;
   std::vector<std::vector<int>> list(G);
   std::vector<std::pair<double, int>> heap;
   for (int c = G - 1; c >= 0; --c) heap.emplace_back(0.0, c);

@@ -233,7 +233,7 @@ def test_attention_schedule_every_item_once_and_balanced(lib, T, H, S, sms):
     G = min(n_items, sms)
     assert len(lists) == G
     assert sorted(u for l in lists for u in l) == list(range(n_items))
-    t_piece = 0.87 / P + 0.02 if P else 0.0
+    t_piece = 0.78 / P + 0.02 if P else 0.0
     cost = lambda u: 1.0 if u < H * n_full else t_piece
     load = [sum(cost(u) for u in l) for l in lists]
     assert max(load) <= sum(load) / G + 1.0 + 1e-9

@@ -189,7 +189,8 @@ def test_convkv_full_shape_sampled_rows():
 
 def test_single_ragged_query_tile_odd_heads():
     """48 tokens per block (one partial query tile per head) and 3 heads:
-    every unit is a half unit; all rows against the oracle."""
+    every item is a per-slot piece of that tile, merged after the kernel;
+    all rows against the oracle."""
     sc = C2_MID.with_(num_heads=3, frames_per_block=3, grid_h=4, grid_w=4)
     keep = {0, 3, 4, 6, 9}
     _, ctxs, outs = H.run_stream(sc, 10, keep, attn_impl=1)

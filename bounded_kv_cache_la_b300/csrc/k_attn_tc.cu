@@ -403,10 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       };
       for (int i = 0; ok; ++i) {
         int h, row0, slot;
-        bool half;
-        if (!units.get(i, h, row0, half, slot)) break;
-        if (half && slot >= n_slots) continue;      // past this context's slots
-        const int s_begin = half ? slot : 0, s_end = half ? slot + 1 : n_slots;
+        bool piece;
+        if (!units.get(i, h, row0, piece, slot)) break;
+        if (piece && slot >= n_slots) continue;      // past this context's slots
+        const int s_begin = piece ? slot : 0, s_end = piece ? slot + 1 : n_slots;
         int j = 0;
         for (int s = s_begin; ok && s < s_end; ++s) {
           const int nt = (cx.tokens[s] + kBN - 1) / kBN;
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             issue_qk(0, ks, qb);
             tc_commit(smem_u32(&ctl.s_full[0]));
             if (j > 0) {
-              if (!half) {
+              if (!piece) {
                 if (!(ok = wait(ctl.p_ready[1], pc1 & 1, 15))) break;
                 tc_fence_after();
                 issue_pv(1, vs, j == 1);
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
               tc_commit(smem_u32(&ctl.v_empty[vs]));
               ++vc;
             }
-            if (!half) {
+            if (!piece) {
               issue_qk(1, ks, qb);
               tc_commit(smem_u32(&ctl.s_full[1]));
             }
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         issue_pv(0, vs, j == 1);
         ++pc0;
         tc_commit(smem_u32(&ctl.o_full[0]));
-        if (!half) {
+        if (!piece) {
           if (!(ok = wait(ctl.p_ready[1], pc1 & 1, 18))) break;
           tc_fence_after();
           issue_pv(1, vs, j == 1);
@@ -497,10 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     bool ok = true;
     for (int i = 0; ok; ++i) {
       int h, row0, slot;
-      bool half;
-      if (!units.get(i, h, row0, half, slot)) break;
-      if (half && (qi == 1 || slot >= n_slots)) continue;   // one tile; past the context
-      const int s_begin = half ? slot : 0, s_end = half ? slot + 1 : n_slots;
+      bool piece;
+      if (!units.get(i, h, row0, piece, slot)) break;
+      if (piece && (qi == 1 || slot >= n_slots)) continue;   // one query tile; past the context
+      const int s_begin = piece ? slot : 0, s_end = piece ? slot + 1 : n_slots;
       const int row = row0 + qi * kBM + r;
       // e4m3: true score = q_scale(row) * k_scale(slot) * S; P is stored as
       // p * v_scale(slot) / v_max so that O = v_max * sum(P V codes).
@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       if (!ok) break;
       ++oph;
       tc_fence_after();
-      if (half) {
+      if (piece) {
         // a piece: v_max * O (unnormalised, fp32), the running max and sum
         const size_t pi = (size_t)h * a.n_pieces + slot;
         float* po = a.part_o + (pi * kBM + r) * kD;

@@ -283,10 +283,12 @@ la_status la_debug_memory(la_cache_t* cache, int layer, void** k_raw, void** v, 
                           int* n_tokens, int* oldest);
 
 /* Profiling: `starts`/`stops` (host arrays of n cudaEvent_t, created by the
- * caller) -- the i-th attention kernel launched after this call records
- * starts[i] immediately before and stops[i] immediately after itself on the
- * caller's stream, for i < n; later launches record nothing.  n = 0 turns
- * recording off.  The arrays are copied; the events stay the caller's. */
+ * caller) -- the i-th attention launched after this call records starts[i]
+ * immediately before it and stops[i] immediately after it on the caller's
+ * stream (the tensor-core attention: its kernel and, when the block has an
+ * odd number of 128-row query tiles, the merge of that tile's per-slot
+ * pieces), for i < n; later launches record nothing.  n = 0 turns recording
+ * off.  The arrays are copied; the events stay the caller's. */
 la_status la_set_profile_events(la_cache_t* cache, void* const* starts, void* const* stops, int n);
 
 /* Failure injection for tests of the failure path (no GPU fault is made).
